@@ -1,0 +1,413 @@
+#!/usr/bin/env python
+"""Benchmark of one denoising step over a 256-position canvas on GB300.
+
+A step is one pass of the whole hot path over one canvas:
+  canvas attention (bidirectional, GQA, over prefix cache + canvas)
+  -> fused vocabulary step (logits, softmax, argmax, confidence,
+     self-conditioning) -> threshold re-noise,
+plus, once per canvas (every `steps` of the workload), the canvas
+initialisation and the incremental KV append of the finished canvas.
+
+Prints ONE JSON line (rank 0). `value` is denoising steps/s over the whole
+job (all ranks; replicas: each rank denoises its own canvas). Inputs are
+seeded synthetic tensors resident in HBM; the embedding table (1.48 GB at
+the headline size) is larger than L2, so no separate L2 flush is needed.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+  python bench.py --impl reference ...   # the CPU oracle on the host cores
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+from canvas_denoising_gb300.configs import HEADLINE, WORKLOADS  # noqa: E402
+
+ORACLE_ROWS = 32  # canvas rows of the vocabulary step the CPU oracle times per step
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=HEADLINE, choices=sorted(WORKLOADS))
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    return ap.parse_args()
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def metric_name():
+    return "denoise steps/s & canvas tok/s (256-pos, V=262144); % of bf16/HBM roofline"
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return {"hbm_gbs": p["hbm_gbs"], "bf16_tflops": p["bf16_tflops"],
+                "bf16_tflops_sustained": p.get("bf16_tflops_sustained"), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+# ---------------------------------------------------------------- clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index):
+        self.proc = None
+        self.lines = []
+        self.dev = device_index
+
+    def start(self):
+        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "100"]
+        uuid = getattr(torch.cuda.get_device_properties(self.dev), "uuid", None)
+        if uuid is not None:
+            s = str(uuid)
+            cmd += ["-i", s if s.startswith("GPU-") else "GPU-" + s]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.th = threading.Thread(target=self._read, daemon=True)
+        self.th.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.th.join(timeout=2)
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+# ---------------------------------------------------------------- workload state on the GPU
+class Canvas:
+    """Everything one rank needs for the denoising loop, resident in HBM."""
+
+    N_INPUTS = 4  # distinct per-step (H, Q, K_c, V_c) sets cycled through
+
+    def __init__(self, w, seed, device):
+        from canvas_denoising_gb300 import binding as B
+        from canvas_denoising_gb300 import synth
+        self.B, self.w = B, w
+        dt = torch.float32 if w.dtype == "f32" else torch.bfloat16
+        self.dt = dt
+        self.seed = seed
+        self.emb = synth.embedding(w.V, w.d, seed, dtype=dt, device=device)
+        self.tgt = synth.targets(w.C, w.V, seed, device=device)
+        self.P = w.prefix
+        self.cap = w.prefix + w.C
+        self.k, self.v = synth.kv_prefix(w.Hkv, self.cap, w.hd, w.prefix, seed, dtype=dt, device=device)
+        self.inputs = []
+        for s in range(self.N_INPUTS):
+            h = synth.hidden(self.emb, self.tgt, w.alpha, seed, step=s, dtype=dt)
+            q, kn, vn = synth.canvas_qkv(w.C, w.Hq, w.Hkv, w.hd, seed, step=s, dtype=dt, device=device)
+            self.inputs.append((h, q, kn, vn))
+        self.tokens = torch.empty(w.C, dtype=torch.int32, device=device)
+        self.renoised = torch.empty(w.C, dtype=torch.uint8, device=device)
+        self.out = torch.empty((w.C, w.Hq, w.hd), dtype=dt, device=device)
+        self.lse_attn = torch.empty((w.Hq, w.C), dtype=torch.float32, device=device)
+        self.argmax = torch.empty(w.C, dtype=torch.int32, device=device)
+        self.conf = torch.empty(w.C, dtype=torch.float32, device=device)
+        self.lse = torch.empty(w.C, dtype=torch.float32, device=device)
+        self.selfcond = torch.empty((w.C, w.d), dtype=dt, device=device)
+        dcode = B.DG_F32 if dt == torch.float32 else B.DG_BF16
+        na = B.canvas_attn_workspace_size(w.C, w.Hq, w.Hkv, w.hd, self.P, dcode)
+        nv = B.vocab_step_workspace_size(w.C, w.V, w.d, dcode)
+        self.ws_attn = torch.empty(max(na, 256), dtype=torch.uint8, device=device)
+        self.ws_vocab = torch.empty(max(nv, 256), dtype=torch.uint8, device=device)
+        self.launches_per_step = None
+
+    def step(self, s, stream, ev=None, inputs=None):
+        """One denoising iteration; per-canvas work at the canvas boundaries."""
+        B, w = self.B, self.w
+        h, q, kn, vn = inputs if inputs is not None else self.inputs[s % self.N_INPUTS]
+        j = s % w.steps
+        n = 0
+        if j == 0:
+            B.canvas_init(self.tokens, w.V, self.seed, self.P, stream=stream)
+            n += 1
+        B.canvas_attn(q, self.k, self.v, self.P, kn, vn, out=self.out, lse=self.lse_attn, workspace=self.ws_attn,
+                      stream=stream)
+        n += 2 if self.ws_attn.numel() > 256 else 1
+        if ev is not None:
+            ev[0].record(stream)
+        B.vocab_step(h, self.emb, argmax=self.argmax, conf=self.conf, lse=self.lse, selfcond=self.selfcond,
+                     workspace=self.ws_vocab, stream=stream)
+        if ev is not None:
+            ev[1].record(stream)
+        n += 2
+        B.renoise(self.tokens, self.argmax, self.conf, w.V, w.thresholds[0], self.seed, j, self.P,
+                  renoised=self.renoised, stream=stream)
+        n += 1
+        if j == w.steps - 1:
+            # finished canvas -> cache rows [P, P+C); the next canvas restarts at the same prefix
+            B.kv_append(self.k, self.v, self.P, kn, vn, stream=stream)
+            n += 1
+        return n
+
+
+def run_ours(args, world, rank, local):
+    from canvas_denoising_gb300 import binding as B
+    from canvas_denoising_gb300 import build as build_mod
+    w = WORKLOADS[args.workload]
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        torch.distributed.init_process_group("nccl", device_id=dev)
+    if not os.path.exists(build_mod.LIB):
+        raise SystemExit("libdgcanvas is not built: run `python -c 'import __graft_entry__ as g; g.build()'` first")
+    B.load()
+    seed = w.seed + rank  # replicas: every rank denoises its own canvas
+    cv = Canvas(w, seed, dev)
+    stream = torch.cuda.Stream(device=dev)
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        for s in range(args.warmup):
+            cv.step(s, stream)
+    stream.synchronize()
+    if B.device_status(stream) != 0:
+        raise SystemExit("device status error after warm-up")
+
+    K = args.steps
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(local)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.3)
+    launches = 0
+    with torch.cuda.stream(stream):
+        t0.record(stream)
+        for s in range(K):
+            launches += cv.step(args.warmup + s, stream, ev=evs[s])
+        t1.record(stream)
+    stream.synchronize()
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    if world > 1:
+        torch.distributed.barrier()
+    ms = t0.elapsed_time(t1)
+    status = B.device_status(stream)
+    vocab_ms = statistics.mean(a.elapsed_time(b) for a, b in evs)
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t.item())
+
+    # ---- end to end through the public API: per-step inputs from pinned host memory, result back
+    e2e = None
+    if not args.no_e2e:
+        Ke = min(K, 200)
+        host_in = [tuple(x.cpu().pin_memory() for x in cv.inputs[i]) for i in range(cv.N_INPUTS)]
+        dev_in = tuple(torch.empty_like(x) for x in cv.inputs[0])
+        host_tok = torch.empty(w.C, dtype=torch.int32).pin_memory()
+        host_sc = torch.empty((w.C, w.d), dtype=cv.dt).pin_memory()
+        h2d = sum(x.numel() * x.element_size() for x in host_in[0])
+        d2h = host_tok.numel() * 4 + host_sc.numel() * host_sc.element_size()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize()
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            for s in range(Ke):
+                for dst, src in zip(dev_in, host_in[s % cv.N_INPUTS]):
+                    dst.copy_(src, non_blocking=True)
+                cv.step(s, stream, inputs=dev_in)
+                host_tok.copy_(cv.tokens, non_blocking=True)
+                host_sc.copy_(cv.selfcond, non_blocking=True)
+            e1.record(stream)
+        stream.synchronize()
+        ems = e0.elapsed_time(e1)
+        if world > 1:
+            t = torch.tensor([ems], device=dev)
+            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+            ems = float(t.item())
+        e2e = {"value": round(world * Ke / (ems / 1e3), 3), "unit": "steps/s", "h2d_bytes_per_step": int(h2d),
+               "d2h_bytes_per_step": int(d2h), "steps": Ke}
+
+    if rank != 0:
+        if world > 1:
+            torch.distributed.destroy_process_group()
+        return None
+    pk = peaks()
+    flops = 4.0 * w.C * w.V * w.d
+    achieved = flops / (vocab_ms / 1e3) / 1e12
+    traffic = committed_traffic("vocab_main", args.workload)
+    roof = {"kernel": "dg_vocab_step (vocab_main + vocab_combine)", "bound": "tensor",
+            "achieved": round(achieved, 1), "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
+            "frac": round(achieved / pk["bf16_tflops"], 4), "traffic": traffic,
+            "peak_source": f"{pk['source']} bf16 burst", "algorithmic_flops_per_launch": flops,
+            "avg_launch_ms": round(vocab_ms, 4)}
+    steps_per_s = world * K / (ms / 1e3)
+    line = {
+        "metric": metric_name(), "value": round(steps_per_s, 3), "unit": "steps/s", "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": round(ms / K, 5), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16" if w.dtype == "bf16" else "f32", "data": "synthetic",
+        "canvas_tok_per_s": round(steps_per_s * w.C, 1),
+        "config": {"workload": w.name, "canvas": w.C, "vocab": w.V, "d_model": w.d, "q_heads": w.Hq,
+                   "kv_heads": w.Hkv, "head_dim": w.hd, "kv_prefix": w.prefix, "threshold": w.thresholds[0],
+                   "steps_per_canvas": w.steps, "alpha": w.alpha, "parallelism": f"replicas{world}",
+                   "l2": "inputs larger than L2 (embedding table %.2f GB), no flush" % (w.V * w.d * 2 / 1e9)},
+        "roofline": roof,
+        "gpu_launches": launches * world,
+        "clocks": clk, "device_status": status,
+    }
+    if e2e is not None:
+        line["e2e"] = e2e
+    if world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(w, cv)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    return line
+
+
+def committed_traffic(kernel, workload):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    from the current source of that kernel (else null)."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        tab = json.load(f)
+    ent = tab.get(kernel, {}).get(workload)
+    if not ent:
+        return None
+    src = os.path.join(ROOT, "canvas_denoising_gb300", "csrc", ent["source"])
+    with open(src, "rb") as f:
+        digest = hashlib.sha256(f.read()).hexdigest()[:16]
+    return ent["bytes_per_launch"] if digest == ent["source_sha256_16"] else None
+
+
+# ---------------------------------------------------------------- CPU oracle arm
+def oracle_step_seconds(w, emb_np, k_np, v_np, inputs_np, rows, seed, step):
+    """Times the oracle on one step: all of attention and re-noise, and the
+    vocabulary step on `rows` canvas rows (rows are independent), scaled to
+    the full canvas."""
+    import oracle
+    h, q, kn, vn = inputs_np
+    t = time.perf_counter()
+    oracle.canvas_attention(q, k_np, v_np, w.prefix, kn, vn)
+    t_attn = time.perf_counter() - t
+    t = time.perf_counter()
+    r = oracle.vocab_step(h[:rows], emb_np, want_top2=False)
+    t_vocab = time.perf_counter() - t
+    t = time.perf_counter()
+    oracle.renoise(np.resize(r["argmax"], w.C), np.resize(r["conf"], w.C).astype(np.float32), w.V, w.thresholds[0],
+                   seed, step, w.prefix)
+    t_rn = time.perf_counter() - t
+    return t_attn + t_rn + t_vocab * (w.C / rows)
+
+
+def _np_inputs(cv, i):
+    return tuple(x.float().cpu().numpy() for x in cv.inputs[i])
+
+
+def cpu_baseline(w, cv):
+    emb_np = cv.emb.float().cpu().numpy()
+    k_np, v_np = cv.k.float().cpu().numpy(), cv.v.float().cpu().numpy()
+    secs = oracle_step_seconds(w, emb_np, k_np, v_np, _np_inputs(cv, 0), ORACLE_ROWS, cv.seed, 0)
+    return {"value": round(1.0 / secs, 5), "unit": "steps/s", "cores": os.cpu_count(), "kind": "oracle",
+            "sample": f"one step: attention and re-noise in full, the vocabulary step on {ORACLE_ROWS} of "
+                      f"{w.C} rows scaled x{w.C // ORACLE_ROWS} (float64 numpy)"}
+
+
+def run_reference(args, world, rank, local):
+    if rank != 0:
+        return None
+    w = WORKLOADS[args.workload]
+    from canvas_denoising_gb300 import synth
+    dt = torch.float32 if w.dtype == "f32" else torch.bfloat16
+    emb = synth.embedding(w.V, w.d, w.seed, dtype=dt)
+    tgt = synth.targets(w.C, w.V, w.seed)
+    k, v = synth.kv_prefix(w.Hkv, w.prefix + w.C, w.hd, w.prefix, w.seed, dtype=dt)
+    emb_np, k_np, v_np = emb.float().numpy(), k.float().numpy(), v.float().numpy()
+    ins = []
+    for s in range(2):
+        h = synth.hidden(emb, tgt, w.alpha, w.seed, step=s, dtype=dt)
+        q, kn, vn = synth.canvas_qkv(w.C, w.Hq, w.Hkv, w.hd, w.seed, step=s, dtype=dt)
+        ins.append(tuple(x.float().numpy() for x in (h, q, kn, vn)))
+    rows = max(1, min(w.C, 8))
+    for s in range(args.warmup):
+        oracle_step_seconds(w, emb_np, k_np, v_np, ins[s % 2], rows, w.seed, s)
+    total = 0.0
+    for s in range(args.steps):
+        total += oracle_step_seconds(w, emb_np, k_np, v_np, ins[s % 2], rows, w.seed, s)
+    val = args.steps / total
+    return {"impl": "reference", "metric": metric_name(), "value": round(val, 6), "unit": "steps/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * total / args.steps, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": w.name, "canvas": w.C, "vocab": w.V, "d_model": w.d, "kv_prefix": w.prefix},
+            "cpu_baseline": {"value": round(val, 6), "unit": "steps/s", "cores": os.cpu_count(), "kind": "oracle",
+                             "sample": f"per step: attention and re-noise in full, the vocabulary step on {rows} of "
+                                       f"{w.C} rows scaled x{w.C / rows:g} (float64 numpy)"},
+            "e2e": {"value": round(val, 6), "unit": "steps/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    args = parse()
+    world, rank, local = dist_env()
+    if args.impl == "reference":
+        line = run_reference(args, world, rank, local)
+    else:
+        line = run_ours(args, world, rank, local)
+    if line is not None:
+        print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,672 @@
+// The fused vocabulary step on the 5th-generation tensor cores (tcgen05).
+//
+// What it computes (DiffusionGemma explainer, "Self-conditioning" and
+// "2. Uniform-state diffusion"): for every canvas row i of H,
+//   l_i = H_i E^T, p_i = softmax(l_i), argmax_i, conf_i = max p_i,
+//   lse_i = log sum exp l_i, S_i = p_i E.
+// The logits never reach memory, and E streams from HBM once per call.
+//
+// Design.
+//  * Fixed per-row reference. softmax(l) = exp(l - R) / sum exp(l - R) for
+//    any R. Each row gets one reference R_i shared by the whole grid, so
+//    every P tile exp(l - R_i) is final the moment its logits exist: P.E
+//    and the row sums accumulate linearly in any order, with no rescaling
+//    of accumulators. R_i is the maximum over a sample of the vocabulary
+//    (every producer CTA's first tile, agreed on through one grid-wide
+//    count). A row whose true maximum exceeds R_i + 40 (exp would leave the
+//    safe fp32 range) is flagged and recomputed exactly by the combine
+//    kernel with R = its true maximum.
+//  * Two CTA roles, one CTA per SM, all co-resident (cooperative launch):
+//    - producer ("A") CTAs own vocabulary tiles of 128 ids (round robin).
+//      GEMM1: logits[rows x 128] = H . E_tile^T, K-loop over d in steps of
+//      64 through a 4-stage TMA ring, two M=128 MMAs per k-step (row halves)
+//      into a double-buffered TMEM accumulator. Four epilogue warps read the
+//      logits from TMEM, keep per-row running max / first argmax / sum of
+//      exp(l - R), and write P = exp(l - R) in bf16 to a global ring,
+//      already in the 128-byte-swizzled K-major layout an MMA operand needs,
+//      then publish the tile with a release flag.
+//    - consumer ("C") CTAs own a [128 rows x 256 d] slice of S and a residue
+//      class of vocabulary tiles. GEMM2: S_slice += P_tile . E_tile[:, slice]
+//      with E read MN-major (the same rows the producer just streamed, so
+//      from L2), accumulating in TMEM over the whole vocabulary. Their fp32
+//      partials go to the workspace once, at the end.
+//  * A combine kernel merges producer statistics (max, lowest argmax, sums)
+//    and consumer partials into argmax, conf, lse and S (bf16).
+// Every wait is bounded (about two seconds of clock); on expiry the kernel
+// latches DG_ERR_TIMEOUT, raises a grid-wide abort flag, drains its own
+// copies and MMAs, frees TMEM and returns.
+#include <cudaTypedefs.h>
+#include <math.h>
+
+#include <mutex>
+
+#include "dg_common.cuh"
+#include "sm100.cuh"
+
+namespace dg {
+namespace {
+
+using namespace sm100;
+
+constexpr int kStages = 4;
+constexpr int kBK = 64;            // d elements per producer k-step (one 128-byte swizzle row)
+constexpr int kVT = 128;           // vocabulary ids per tile
+constexpr int kDT = 256;           // S columns per consumer CTA
+constexpr int kThreads = 192;      // warp 0: TMA, warp 1: MMA, warps 2..5: epilogue
+constexpr uint32_t kStageBytes = 48u * 1024u;
+constexpr uint32_t kTileBytes = 16384u;  // [128 rows x 64 bf16], one swizzled operand block
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kTau = 40.f;       // overflow margin above the reference, natural log
+constexpr long long kTimeoutCycles = 4000000000ll;
+
+struct Plan {
+  int n_rh, n_dt, n_vt, ksplit, n_a, n_c;
+};
+
+int num_sms() {
+  static int n = 0;
+  if (!n) {
+    int dev = 0, v = 0;
+    if (cudaGetDevice(&dev) == cudaSuccess &&
+        cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && v > 0)
+      n = v;
+    else
+      n = 152;
+  }
+  return n;
+}
+
+Plan make_plan(int C, int V, int d) {
+  Plan p;
+  p.n_rh = (C + 127) / 128;
+  p.n_dt = (d + kDT - 1) / kDT;
+  p.n_vt = (V + kVT - 1) / kVT;
+  const int sms = num_sms();
+  const int tiles_c = p.n_rh * p.n_dt;
+  int ks = (int)lround((double)(sms / 2) / tiles_c);
+  if (ks < 1) ks = 1;
+  if (ks > p.n_vt) ks = p.n_vt;
+  while (ks > 1 && tiles_c * ks > sms - 1) --ks;
+  p.ksplit = ks;
+  p.n_c = tiles_c * ks;
+  p.n_a = sms - p.n_c;
+  if (p.n_a > p.n_vt) p.n_a = p.n_vt;
+  if (p.n_a < 1) p.n_a = 1;
+  return p;
+}
+
+struct Layout {
+  size_t flags, smax, am, aa, az, cpart, pbuf, total;
+  size_t flag_bytes;
+};
+
+size_t up256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+Layout make_layout(const Plan& p, int d) {
+  Layout L;
+  size_t o = 0;
+  L.flags = o;
+  L.flag_bytes = (size_t)(p.n_vt + 2 + 256) * sizeof(int);
+  o += up256(L.flag_bytes);
+  L.smax = o; o += up256((size_t)p.n_a * 256 * 4);
+  L.am = o;   o += up256((size_t)p.n_a * 256 * 4);
+  L.aa = o;   o += up256((size_t)p.n_a * 256 * 4);
+  L.az = o;   o += up256((size_t)p.n_a * 256 * 4);
+  L.cpart = o; o += up256((size_t)p.ksplit * 256 * d * 4);
+  L.pbuf = o; o += (size_t)p.n_vt * p.n_rh * 2 * kTileBytes;
+  L.total = o;
+  return L;
+}
+
+struct Params {
+  int C, V, d, n_rh, n_dt, n_vt, ksplit, n_a;
+  int* ready;      // [n_vt] tile published counters
+  int* ref_count;  // producers that have published their sample maxima
+  int* abort_flag;
+  int* overflow;   // [256]
+  float* smax;     // [n_a][256] sample maxima
+  float* am;       // [n_a][256] running max
+  int* aa;         // [n_a][256] first argmax
+  float* az;       // [n_a][256] sum of exp(l - R)
+  float* cpart;    // [ksplit][256][d]
+  uint8_t* pbuf;   // [n_vt][n_rh][2][16 KB]
+  int* status;
+};
+
+__device__ __forceinline__ bool aborted(const int* f) { return *(volatile const int*)f != 0; }
+
+__device__ __forceinline__ void raise_abort(const Params& p) {
+  atomicExch(p.abort_flag, 1);
+  latch(p.status, DG_ERR_TIMEOUT);
+}
+
+// Bounded mbarrier wait: false on timeout (abort raised) or if another CTA aborted.
+__device__ bool wait_bar(uint32_t bar, uint32_t parity, const Params& p) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const long long t0 = clock64();
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((it & 255u) == 0) {
+      if (aborted(p.abort_flag)) return false;
+      if (clock64() - t0 > kTimeoutCycles) {
+        raise_abort(p);
+        return false;
+      }
+    }
+  }
+}
+
+// Bounded wait until *flag >= target (acquire).
+__device__ bool wait_flag(const int* flag, int target, const Params& p) {
+  const long long t0 = clock64();
+  for (uint32_t it = 0;; ++it) {
+    if ((int)ld_acquire_gpu(flag) >= target) return true;
+    if (aborted(p.abort_flag)) return false;
+    if (clock64() - t0 > kTimeoutCycles) {
+      raise_abort(p);
+      return false;
+    }
+    __nanosleep(64);
+  }
+}
+
+__device__ __forceinline__ void epi_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+
+// Barrier over the 128 epilogue threads that also ORs a predicate across them,
+// so that every epilogue thread takes the same branch after a bounded wait.
+__device__ __forceinline__ bool epi_any(bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n .reg .pred pi, po;\n setp.ne.u32 pi, %1, 0;\n barrier.red.or.pred po, 1, 128, pi;\n"
+      " selp.u32 %0, 1, 0, po;\n}\n"
+      : "=r"(r)
+      : "r"((uint32_t)v)
+      : "memory");
+  return r != 0;
+}
+
+__device__ __forceinline__ uint32_t pack2(float a, float b) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    vocab_main(const __grid_constant__ CUtensorMap tm_h, const __grid_constant__ CUtensorMap tm_ek,
+               const __grid_constant__ CUtensorMap tm_emn, const Params p) {
+  extern __shared__ __align__(1024) uint8_t smem_dyn[];
+  __shared__ __align__(8) uint64_t bar_full[kStages], bar_empty[kStages], bar_tfull[2], bar_tempty[2], bar_drain;
+  __shared__ uint32_t tmem_slot;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  uint8_t* stages = (uint8_t*)(((uintptr_t)smem_dyn + 1023) & ~(uintptr_t)1023);
+  const uint32_t s_base = smem_addr(stages);
+  const bool is_a = (int)blockIdx.x < p.n_a;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(smem_addr(&bar_full[s]), 1);
+      mbar_init(smem_addr(&bar_empty[s]), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(smem_addr(&bar_tfull[b]), 1);
+      mbar_init(smem_addr(&bar_tempty[b]), 128);
+    }
+    mbar_init(smem_addr(&bar_drain), 1);
+    fence_mbar_init();
+    prefetch_tmap(&tm_h);
+    prefetch_tmap(&tm_ek);
+    prefetch_tmap(&tm_emn);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_addr(&tmem_slot), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_slot;
+  const int ksteps_d = p.d / kBK;
+
+  if (is_a) {
+    // ===================================================== producer role: GEMM1 + softmax epilogue
+    const int a = blockIdx.x;
+    const int n_my = a < p.n_vt ? (p.n_vt - a + p.n_a - 1) / p.n_a : 0;
+    if (warp == 0) {
+      if (lane == 0 && n_my > 0) {
+        int stage = 0;
+        uint32_t ph = 0;
+        uint32_t issued_par[kStages];
+        bool issued[kStages];
+        for (int s = 0; s < kStages; ++s) issued[s] = false, issued_par[s] = 0;
+        const uint32_t tx = (uint32_t)(p.n_rh + 1) * kTileBytes;
+        bool ok = true;
+        for (int j = 0; j < n_my && ok; ++j) {
+          const int t = a + j * p.n_a;
+          for (int ks = 0; ks < ksteps_d; ++ks) {
+            if (!wait_bar(smem_addr(&bar_empty[stage]), ph ^ 1, p)) { ok = false; break; }
+            const uint32_t fb = smem_addr(&bar_full[stage]);
+            const uint32_t sb = s_base + stage * kStageBytes;
+            mbar_expect_tx(fb, tx);
+            for (int h = 0; h < p.n_rh; ++h) tma_load_2d(sb + h * kTileBytes, &tm_h, ks * kBK, h * 128, fb);
+            tma_load_2d(sb + 2 * kTileBytes, &tm_ek, ks * kBK, t * kVT, fb);
+            issued[stage] = true;
+            issued_par[stage] = ph;
+            if (++stage == kStages) { stage = 0; ph ^= 1; }
+          }
+        }
+        // drain: every copy this thread issued has landed before the CTA may exit
+        for (int s = 0; s < kStages; ++s)
+          if (issued[s]) wait_bar(smem_addr(&bar_full[s]), issued_par[s], p);
+      }
+      __syncwarp();
+    } else if (warp == 1) {
+      if (lane == 0 && n_my > 0) {
+        const uint32_t idesc = idesc_bf16_f32(128, kVT, 0, 0);
+        int stage = 0;
+        uint32_t ph = 0;
+        bool ok = true;
+        for (int j = 0; j < n_my && ok; ++j) {
+          const int b = j & 1;
+          const uint32_t u = (uint32_t)(j >> 1);
+          if (!wait_bar(smem_addr(&bar_tempty[b]), (u & 1) ^ 1, p)) break;
+          tc_fence_after();
+          for (int ks = 0; ks < ksteps_d; ++ks) {
+            if (!wait_bar(smem_addr(&bar_full[stage]), ph, p)) { ok = false; break; }
+            tc_fence_after();
+            const uint32_t sb = s_base + stage * kStageBytes;
+#pragma unroll
+            for (int k = 0; k < kBK / 16; ++k) {
+              const uint64_t bdesc = sdesc_sw128(sb + 2 * kTileBytes + k * 32, 0, 1024);
+              for (int h = 0; h < p.n_rh; ++h) {
+                const uint64_t adesc = sdesc_sw128(sb + h * kTileBytes + k * 32, 0, 1024);
+                mma_bf16(tmem + b * 256 + h * 128, adesc, bdesc, idesc, (ks | k) != 0);
+              }
+            }
+            mma_commit(smem_addr(&bar_empty[stage]));
+            if (++stage == kStages) { stage = 0; ph ^= 1; }
+          }
+          if (ok) mma_commit(smem_addr(&bar_tfull[b]));
+        }
+        mma_commit(smem_addr(&bar_drain));
+        wait_bar(smem_addr(&bar_drain), 0, p);
+      }
+      __syncwarp();
+    } else {
+      // epilogue warps 2..5: TMEM lane quarter q = warp % 4, one row per thread per row half
+      const int q = warp & 3;
+      const int r = q * 32 + lane;
+      const uint32_t lane_off = (uint32_t)(q * 32) << 16;
+      float R2[2] = {0.f, 0.f}, Rn[2] = {0.f, 0.f};
+      float m_run[2] = {-INFINITY, -INFINITY}, z_run[2] = {0.f, 0.f};
+      int a_run[2] = {0x7fffffff, 0x7fffffff};
+      bool ovf[2] = {false, false};
+      bool ok = true;
+      if (n_my == 0) {
+        for (int h = 0; h < 2; ++h) p.smax[(size_t)a * 256 + h * 128 + r] = -INFINITY;
+        __threadfence();
+        epi_sync();
+        if (threadIdx.x == 64) red_release_add_gpu(p.ref_count, 1);
+      }
+      for (int j = 0; j < n_my && ok; ++j) {
+        const int b = j & 1;
+        const uint32_t u = (uint32_t)(j >> 1);
+        const int t = a + j * p.n_a;
+        const bool got = wait_bar(smem_addr(&bar_tfull[b]), u & 1, p);
+        if (epi_any(!got)) { ok = false; break; }
+        tc_fence_after();
+        if (j == 0) {
+          // sample maxima of this CTA's first tile -> grid-wide reference
+          for (int h = 0; h < 2; ++h) {
+            float mx = -INFINITY;
+            if (h < p.n_rh) {
+              for (int c = 0; c < kVT / 32; ++c) {
+                float v[32];
+                tmem_ld32(tmem + lane_off + b * 256 + h * 128 + c * 32, v);
+#pragma unroll
+                for (int e = 0; e < 32; ++e)
+                  if (t * kVT + c * 32 + e < p.V) mx = fmaxf(mx, v[e]);
+              }
+            }
+            p.smax[(size_t)a * 256 + h * 128 + r] = mx;
+          }
+          __threadfence();
+          epi_sync();
+          if (threadIdx.x == 64) red_release_add_gpu(p.ref_count, 1);
+          const bool refd = wait_flag(p.ref_count, p.n_a, p);
+          if (epi_any(!refd)) { ok = false; break; }
+          for (int h = 0; h < 2; ++h) {
+            float R = -INFINITY;
+            for (int aa = 0; aa < p.n_a; ++aa) R = fmaxf(R, __ldcg(p.smax + (size_t)aa * 256 + h * 128 + r));
+            Rn[h] = R;
+            R2[h] = R * kLog2e;
+          }
+        }
+        for (int h = 0; h < p.n_rh; ++h) {
+          const float lim2 = (Rn[h] + kTau) * kLog2e;
+          for (int c = 0; c < kVT / 32; ++c) {
+            float v[32];
+            tmem_ld32(tmem + lane_off + b * 256 + h * 128 + c * 32, v);
+            const int vbase = t * kVT + c * 32;
+            uint32_t pk[16];
+#pragma unroll
+            for (int e = 0; e < 32; e += 2) {
+              float pe[2];
+#pragma unroll
+              for (int f = 0; f < 2; ++f) {
+                const float l = v[e + f];
+                const int id = vbase + e + f;
+                float pv = 0.f;
+                if (id < p.V) {
+                  if (l > m_run[h]) { m_run[h] = l; a_run[h] = id; }
+                  const float x2 = l * kLog2e;
+                  if (x2 > lim2) ovf[h] = true;
+                  pv = exp2f(x2 - R2[h]);
+                  z_run[h] += pv;
+                }
+                pe[f] = pv;
+              }
+              pk[e >> 1] = pack2(pe[0], pe[1]);
+            }
+            uint8_t* dst = p.pbuf + ((size_t)(t * p.n_rh + h) * 2 + (c >> 1)) * kTileBytes + (size_t)r * 128;
+#pragma unroll
+            for (int jj = 0; jj < 4; ++jj) {
+              const int chunk = (c & 1) * 4 + jj;
+              uint4 w = make_uint4(pk[jj * 4 + 0], pk[jj * 4 + 1], pk[jj * 4 + 2], pk[jj * 4 + 3]);
+              *reinterpret_cast<uint4*>(dst + ((chunk ^ (r & 7)) << 4)) = w;
+            }
+          }
+        }
+        tc_fence_before();
+        mbar_arrive(smem_addr(&bar_tempty[b]));
+        // publish the P tile to consumer CTAs (generic writes -> async-proxy reads elsewhere)
+        fence_proxy_async_global();
+        __threadfence();
+        epi_sync();
+        if (threadIdx.x == 64) red_release_add_gpu(p.ready + t, 1);
+      }
+      for (int h = 0; h < p.n_rh; ++h) {
+        const int i = h * 128 + r;
+        if (i < p.C) {
+          p.am[(size_t)a * 256 + i] = m_run[h];
+          p.aa[(size_t)a * 256 + i] = a_run[h];
+          p.az[(size_t)a * 256 + i] = z_run[h];
+          if (ovf[h]) p.overflow[i] = 1;
+        }
+      }
+    }
+  } else {
+    // ===================================================== consumer role: GEMM2 (S += P . E)
+    const int c = blockIdx.x - p.n_a;
+    const int tau = c % p.n_dt;
+    const int h = (c / p.n_dt) % p.n_rh;
+    const int kap = c / (p.n_dt * p.n_rh);
+    const int d0 = tau * kDT;
+    const int nd = p.d - d0 < kDT ? p.d - d0 : kDT;
+    const int nbox = nd / 64;
+    const int n_my = kap < p.n_vt ? (p.n_vt - kap + p.ksplit - 1) / p.ksplit : 0;
+    if (warp == 0) {
+      if (lane == 0 && n_my > 0) {
+        int stage = 0;
+        uint32_t ph = 0;
+        uint32_t issued_par[kStages];
+        bool issued[kStages];
+        for (int s = 0; s < kStages; ++s) issued[s] = false, issued_par[s] = 0;
+        const uint32_t tx = kTileBytes + (uint32_t)nbox * 8192u;
+        bool ok = true;
+        for (int j = 0; j < n_my && ok; ++j) {
+          const int t = kap + j * p.ksplit;
+          if (!wait_flag(p.ready + t, 1, p)) break;
+          fence_proxy_async_global();
+          for (int ks = 0; ks < 2; ++ks) {
+            if (!wait_bar(smem_addr(&bar_empty[stage]), ph ^ 1, p)) { ok = false; break; }
+            const uint32_t fb = smem_addr(&bar_full[stage]);
+            const uint32_t sb = s_base + stage * kStageBytes;
+            mbar_expect_tx(fb, tx);
+            bulk_load(sb, p.pbuf + ((size_t)(t * p.n_rh + h) * 2 + ks) * kTileBytes, kTileBytes, fb);
+            for (int bx = 0; bx < nbox; ++bx)
+              tma_load_2d(sb + kTileBytes + bx * 8192, &tm_emn, d0 + bx * 64, t * kVT + ks * 64, fb);
+            issued[stage] = true;
+            issued_par[stage] = ph;
+            if (++stage == kStages) { stage = 0; ph ^= 1; }
+          }
+        }
+        for (int s = 0; s < kStages; ++s)
+          if (issued[s]) wait_bar(smem_addr(&bar_full[s]), issued_par[s], p);
+      }
+      __syncwarp();
+    } else if (warp == 1) {
+      if (lane == 0 && n_my > 0) {
+        const uint32_t idesc = idesc_bf16_f32(128, nd, 0, 1);
+        int stage = 0;
+        uint32_t ph = 0;
+        bool ok = true, first = true;
+        for (int j = 0; j < n_my && ok; ++j) {
+          for (int ks = 0; ks < 2; ++ks) {
+            if (!wait_bar(smem_addr(&bar_full[stage]), ph, p)) { ok = false; break; }
+            tc_fence_after();
+            const uint32_t sb = s_base + stage * kStageBytes;
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              const uint64_t adesc = sdesc_sw128(sb + k * 32, 0, 1024);
+              const uint64_t bdesc = sdesc_sw128(sb + kTileBytes + k * 2048, 8192, 1024);
+              mma_bf16(tmem, adesc, bdesc, idesc, first ? 0u : 1u);
+              first = false;
+            }
+            mma_commit(smem_addr(&bar_empty[stage]));
+            if (++stage == kStages) { stage = 0; ph ^= 1; }
+          }
+        }
+        mma_commit(smem_addr(&bar_tfull[0]));
+        wait_bar(smem_addr(&bar_tfull[0]), 0, p);
+      }
+      __syncwarp();
+    } else {
+      const int q = warp & 3;
+      const int r = q * 32 + lane;
+      const int i = h * 128 + r;
+      const uint32_t lane_off = (uint32_t)(q * 32) << 16;
+      float* dst = p.cpart + ((size_t)kap * 256 + i) * p.d + d0;
+      bool have = n_my > 0;
+      if (have) {
+        have = wait_bar(smem_addr(&bar_tfull[0]), 0, p);
+        have = __all_sync(0xffffffffu, have);  // tcgen05.ld below is warp-collective
+        tc_fence_after();
+      }
+      for (int cc = 0; cc < nd / 32; ++cc) {
+        float v[32];
+        if (have) {
+          tmem_ld32(tmem + lane_off + cc * 32, v);
+        } else {
+#pragma unroll
+          for (int e = 0; e < 32; ++e) v[e] = 0.f;
+        }
+        if (i < p.C) {
+#pragma unroll
+          for (int e = 0; e < 32; e += 4)
+            *reinterpret_cast<float4*>(dst + cc * 32 + e) = make_float4(v[e], v[e + 1], v[e + 2], v[e + 3]);
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+// Merge producer statistics and consumer partials for one canvas row (and one
+// 256-column slice of S). A row flagged by the producers is recomputed here
+// from scratch with its true maximum as the reference (fp32, CUDA cores).
+__global__ void __launch_bounds__(256) vocab_combine(const Params p, const __nv_bfloat16* __restrict__ h,
+                                                     const __nv_bfloat16* __restrict__ emb, int32_t* argmax,
+                                                     float* conf, float* lse, __nv_bfloat16* selfcond) {
+  extern __shared__ float hrow[];  // [d] (fixup only)
+  __shared__ float s_m[8], s_z[8], s_r[8], s_pv[256];
+  __shared__ int s_a[8];
+  const int i = blockIdx.x, slice = blockIdx.y, t = threadIdx.x, lane = t & 31, w = t >> 5;
+  float m = -INFINITY, z = 0.f, R = -INFINITY;
+  int ai = 0x7fffffff;
+  for (int a = t; a < p.n_a; a += 256) {
+    const float ma = p.am[(size_t)a * 256 + i];
+    const int aa = p.aa[(size_t)a * 256 + i];
+    z += p.az[(size_t)a * 256 + i];
+    R = fmaxf(R, p.smax[(size_t)a * 256 + i]);
+    if (ma > m || (ma == m && aa < ai)) { m = ma; ai = aa; }
+  }
+  for (int o = 16; o; o >>= 1) {
+    const float om = __shfl_xor_sync(0xffffffffu, m, o);
+    const int oa = __shfl_xor_sync(0xffffffffu, ai, o);
+    if (om > m || (om == m && oa < ai)) { m = om; ai = oa; }
+    z += __shfl_xor_sync(0xffffffffu, z, o);
+    R = fmaxf(R, __shfl_xor_sync(0xffffffffu, R, o));
+  }
+  if (lane == 0) { s_m[w] = m; s_a[w] = ai; s_z[w] = z; s_r[w] = R; }
+  __syncthreads();
+  m = s_m[0]; ai = s_a[0]; z = s_z[0]; R = s_r[0];
+  for (int k = 1; k < 8; ++k) {
+    if (s_m[k] > m || (s_m[k] == m && s_a[k] < ai)) { m = s_m[k]; ai = s_a[k]; }
+    z += s_z[k];
+    R = fmaxf(R, s_r[k]);
+  }
+  __syncthreads();
+  const int j = slice * 256 + t;
+  const bool ovf = p.overflow[i] != 0;
+  float out_conf, out_lse;
+  if (!ovf) {
+    out_conf = expf(m - R) / z;
+    out_lse = R + logf(z);
+    if (selfcond && j < p.d) {
+      float acc = 0.f;
+      for (int k = 0; k < p.ksplit; ++k) acc += p.cpart[((size_t)k * 256 + i) * p.d + j];
+      selfcond[(size_t)i * p.d + j] = __float2bfloat16_rn(acc / z);
+    }
+  } else {
+    // exact recompute with R = m (the row's true maximum)
+    for (int k = t; k < p.d; k += 256) hrow[k] = __bfloat162float(h[(size_t)i * p.d + k]);
+    __syncthreads();
+    float zp = 0.f, acc = 0.f;
+    for (int v0 = 0; v0 < p.V; v0 += 256) {
+      for (int vv = w * 32; vv < w * 32 + 32; ++vv) {
+        const int v = v0 + vv;
+        float dot = 0.f;
+        if (v < p.V)
+          for (int k = lane; k < p.d; k += 32) dot = fmaf(hrow[k], __bfloat162float(emb[(size_t)v * p.d + k]), dot);
+        for (int o = 16; o; o >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, o);
+        if (lane == 0) s_pv[vv] = v < p.V ? expf(dot - m) : 0.f;
+      }
+      __syncthreads();
+      zp += s_pv[t];
+      if (j < p.d) {
+        const int nv = p.V - v0 < 256 ? p.V - v0 : 256;
+        for (int vv = 0; vv < nv; ++vv) acc = fmaf(s_pv[vv], __bfloat162float(emb[(size_t)(v0 + vv) * p.d + j]), acc);
+      }
+      __syncthreads();
+    }
+    for (int o = 16; o; o >>= 1) zp += __shfl_xor_sync(0xffffffffu, zp, o);
+    if (lane == 0) s_z[w] = zp;
+    __syncthreads();
+    zp = 0.f;
+    for (int k = 0; k < 8; ++k) zp += s_z[k];
+    out_conf = 1.f / zp;
+    out_lse = m + logf(zp);
+    if (selfcond && j < p.d) selfcond[(size_t)i * p.d + j] = __float2bfloat16_rn(acc / zp);
+  }
+  if (slice == 0 && t == 0) {
+    argmax[i] = ai;
+    conf[i] = out_conf;
+    if (lse) lse[i] = out_lse;
+  }
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static std::once_flag once;
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = (PFN_cuTensorMapEncodeTiled_v12000)f;
+  });
+  return fn;
+}
+
+// 2D bf16 map over a row-major [rows][cols] matrix, box [box_rows][64], 128-byte swizzle.
+bool make_map(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows, uint32_t box_rows) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols * 2};
+  cuuint32_t box[2] = {64, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+size_t vocab_tc_workspace(int C, int V, int d) {
+  Plan pl = make_plan(C, V, d);
+  return make_layout(pl, d).total;
+}
+
+int vocab_tc_launch(const __nv_bfloat16* h, const __nv_bfloat16* emb, int C, int V, int d, int32_t* argmax,
+                    float* conf, float* lse, __nv_bfloat16* selfcond, void* ws, size_t ws_bytes, cudaStream_t s) {
+  const Plan pl = make_plan(C, V, d);
+  const Layout L = make_layout(pl, d);
+  if (ws_bytes < L.total) return DG_ERR_WORKSPACE;
+  int* st = status_ptr();
+  if (!st) return DG_ERR_CUDA;
+  CUtensorMap tm_h, tm_ek, tm_emn;
+  if (!make_map(&tm_h, h, d, C, 128) || !make_map(&tm_ek, emb, d, V, 128) || !make_map(&tm_emn, emb, d, V, 64))
+    return DG_ERR_CUDA;
+  uint8_t* w = (uint8_t*)ws;
+  Params p;
+  p.C = C; p.V = V; p.d = d;
+  p.n_rh = pl.n_rh; p.n_dt = pl.n_dt; p.n_vt = pl.n_vt; p.ksplit = pl.ksplit; p.n_a = pl.n_a;
+  int* flags = (int*)(w + L.flags);
+  p.ready = flags;
+  p.ref_count = flags + pl.n_vt;
+  p.abort_flag = flags + pl.n_vt + 1;
+  p.overflow = flags + pl.n_vt + 2;
+  p.smax = (float*)(w + L.smax);
+  p.am = (float*)(w + L.am);
+  p.aa = (int*)(w + L.aa);
+  p.az = (float*)(w + L.az);
+  p.cpart = (float*)(w + L.cpart);
+  p.pbuf = w + L.pbuf;
+  p.status = st;
+  DG_CUDA_TRY(cudaMemsetAsync(flags, 0, L.flag_bytes, s));
+
+  const size_t smem = (size_t)kStages * kStageBytes + 1024;
+  static std::once_flag attr_once;
+  static cudaError_t attr_err = cudaSuccess;
+  std::call_once(attr_once, [&] {
+    attr_err = cudaFuncSetAttribute(vocab_main, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  });
+  DG_CUDA_TRY(attr_err);
+
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(pl.n_a + pl.n_c);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  DG_CUDA_TRY(cudaLaunchKernelEx(&cfg, vocab_main, tm_h, tm_ek, tm_emn, p));
+
+  dim3 cgrid(C, pl.n_dt);
+  const size_t csmem = (size_t)d * sizeof(float);
+  vocab_combine<<<cgrid, 256, csmem, s>>>(p, h, emb, argmax, conf, lse, selfcond);
+  DG_LAUNCH_CHECK();
+  return DG_OK;
+}
+
+}  // namespace dg

@@ -1,0 +1,158 @@
+/*
+ * dg_canvas.h -- C ABI of libdgcanvas, the GB300 (sm_103a) hot path of one
+ * uniform-state text-diffusion denoising step over a fixed-size canvas.
+ *
+ * Source of each operation: the DiffusionGemma explainer ("Understanding
+ * DiffusionGemma", ai.google.dev/gemma/docs/diffusiongemma/explained):
+ *   dg_canvas_attn   -- "Architecture: incremental prefill and denoising",
+ *                       denoising mode: every canvas query attends to every
+ *                       canvas token and to the KV cache (bidirectional).
+ *   dg_vocab_step    -- "2. Uniform-state diffusion" (a token's probability
+ *                       against a threshold) and "Self-conditioning" (the
+ *                       probability matrix times the token-embedding table).
+ *   dg_renoise       -- "2. Uniform-state diffusion": a token whose
+ *                       probability falls below the threshold is replaced by
+ *                       a random vocabulary token.
+ *   dg_canvas_init   -- "The problem with autoregressive models": the canvas
+ *                       starts as random tokens drawn from the vocabulary.
+ *   dg_kv_append     -- "Architecture..." prefill mode and "Multi-canvas
+ *                       sampling": each finalised canvas is appended to the
+ *                       KV cache with causal attention.
+ *
+ * Conventions shared by every call
+ *   - Pointers named as tensors are DEVICE pointers owned by the caller, in
+ *     the layout stated beside them (row-major, densely packed). `stream` is
+ *     a cudaStream_t (NULL = the legacy default stream). Calls are
+ *     asynchronous on `stream`.
+ *   - Host-side validation runs first. On any error no kernel is launched and
+ *     no output is touched; the call returns the error.
+ *   - A launch failure returns DG_ERR_CUDA. Faults a kernel detects itself
+ *     (a bounded wait that ran out, an index out of range) are latched into a
+ *     library-owned device status word, read and cleared by dg_device_status.
+ *     Kernels never trap.
+ *   - The library allocates nothing per call. Scratch memory is the caller's
+ *     workspace, sized by the *_workspace_size queries (0 is a valid size).
+ *     A workspace must be 256-byte aligned and must not be shared by calls
+ *     that can run concurrently.
+ *   - dtype DG_BF16: bf16 tensors, fp32 accumulation and softmax; this is the
+ *     tensor-core (tcgen05) path. dtype DG_F32: fp32 tensors, a CUDA-core
+ *     path meant for small shapes.
+ */
+#ifndef DG_CANVAS_H
+#define DG_CANVAS_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define DG_API __attribute__((visibility("default")))
+#else
+#define DG_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  DG_OK = 0,
+  DG_ERR_INVALID_ARG = -1,   /* null/misaligned pointer, bad size, len+C > cap ... */
+  DG_ERR_UNSUPPORTED = -2,   /* shape or dtype this build does not implement      */
+  DG_ERR_WORKSPACE = -3,     /* workspace smaller than the size query returned    */
+  DG_ERR_CUDA = -4,          /* a CUDA runtime call or launch failed              */
+  DG_ERR_TIMEOUT = -5,       /* (device status) a bounded wait ran out            */
+  DG_ERR_DEVICE_BOUNDS = -6  /* (device status) a kernel saw an index out of range */
+} dg_status;
+
+typedef enum { DG_BF16 = 0, DG_F32 = 1 } dg_dtype;
+
+typedef enum {
+  DG_MASK_BIDIR = 0,        /* denoising: no mask                                      */
+  DG_MASK_CAUSAL_BLOCK = 1  /* prefill: query i (absolute position P+i) sees keys 0..P+i */
+} dg_mask;
+
+/* Human-readable name of a status code. Never NULL. */
+DG_API const char* dg_status_string(int status);
+
+/* Synchronises `stream`, then returns the device status word (DG_OK or the
+ * first DG_ERR_TIMEOUT / DG_ERR_DEVICE_BOUNDS latched since the last call)
+ * and clears it. Returns DG_ERR_CUDA if the synchronisation itself fails. */
+DG_API int dg_device_status(void* stream);
+
+/* ---------------------------------------------------------------- attention
+ * Canvas attention (denoising mode), grouped-query:
+ *   for query head h (KV head g = h / (Hq/Hkv)) and canvas position i,
+ *   keys/values = [cache rows 0..P-1 of head g ; canvas rows 0..C-1 of head g]
+ *   out[i][h]  = softmax_j(q[i][h] . k_j * scale) . v
+ *   lse[h][i]  = natural-log log-sum-exp of the scaled scores
+ *
+ *   q         [C][Hq][hd]        k_cache, v_cache [Hkv][cap][hd] (rows [0,P) read)
+ *   k_canvas  [Hkv][C][hd]       v_canvas [Hkv][C][hd]
+ *   out       [C][Hq][hd] (dtype)   lse [Hq][C] fp32, or NULL
+ *   scale <= 0 selects 1/sqrt(hd). mask = dg_mask.
+ * Requirements: Hq % Hkv == 0; hd in {32, 64, 128}; 0 <= P <= cap; C >= 1;
+ * every pointer 16-byte aligned. Workspace: split-KV partials.
+ */
+DG_API size_t dg_canvas_attn_workspace_size(int C, int Hq, int Hkv, int hd, int64_t prefix_len, int dtype);
+DG_API int dg_canvas_attn(const void* q, const void* k_cache, const void* v_cache, int64_t cap, int64_t prefix_len,
+                   const void* k_canvas, const void* v_canvas, void* out, float* lse,
+                   int C, int Hq, int Hkv, int hd, float scale, int dtype, int mask,
+                   void* workspace, size_t workspace_bytes, void* stream);
+
+/* ---------------------------------------------------------------- vocabulary step
+ * For each canvas position i (row of h):
+ *   logits l_i = h_i . emb^T            (emb is the tied token-embedding table)
+ *   argmax[i]  = lowest vocabulary id attaining max_v l_iv
+ *   conf[i]    = softmax(l_i)[argmax[i]] = 1 / sum_v exp(l_iv - max l_i)
+ *   lse[i]     = log-sum-exp of l_i (natural log)
+ *   selfcond[i]= softmax(l_i) . emb     (the self-conditioning vector)
+ * One streaming pass over vocabulary tiles; the logits never reach memory.
+ *
+ *   h        [C][d] (dtype)     emb [V][d] (dtype)
+ *   argmax   [C] int32          conf [C] fp32      lse [C] fp32 or NULL
+ *   selfcond [C][d] (dtype) or NULL
+ * Requirements (DG_BF16): 1 <= C <= 256, d % 64 == 0, 64 <= d <= 8192, V >= 1.
+ * (DG_F32): C >= 1, 1 <= V <= 16384, 1 <= d <= 1024.
+ */
+DG_API size_t dg_vocab_step_workspace_size(int C, int V, int d, int dtype);
+DG_API int dg_vocab_step(const void* h, const void* emb, int C, int V, int d, int dtype,
+                  int32_t* argmax, float* conf, float* lse, void* selfcond,
+                  void* workspace, size_t workspace_bytes, void* stream);
+
+/* ---------------------------------------------------------------- re-noise
+ * tokens[i] = conf[i] < threshold ? U(seed, step, abs_pos0 + i) : argmax[i]
+ * renoised[i] = (conf[i] < threshold)            (renoised may be NULL)
+ * U is a uniform vocabulary id: Philox4x64-10 with key (seed, 0) and counter
+ * (absolute position, step, 0, 0); output word 0, mapped to [0, V) as
+ * ((word >> 32) * V) >> 32. The comparison is in fp32 and strict.
+ *   tokens [C] int32 (out; may alias nothing else)   argmax [C] int32   conf [C] fp32
+ * Requirements: C >= 1, 1 <= V <= 2^31 - 1. An argmax outside [0, V) is copied
+ * as is and latches DG_ERR_DEVICE_BOUNDS.
+ */
+DG_API int dg_renoise(int32_t* tokens, const int32_t* argmax, const float* conf, int C, int V, float threshold,
+               uint64_t seed, uint32_t step, int64_t abs_pos0, uint8_t* renoised, void* stream);
+
+/* Fresh canvas: tokens[i] = U_init(seed, abs_pos0 + i): the same Philox draw
+ * with counter (absolute position, 0, 1, 0). */
+DG_API int dg_canvas_init(int32_t* tokens, int C, int V, uint64_t seed, int64_t abs_pos0, void* stream);
+
+/* ---------------------------------------------------------------- KV append
+ * Incremental causal prefill of one finalised canvas:
+ *   k_cache[g][*len + i] = k_new[g][i], v_cache likewise, for i < C, all g;
+ *   then *len += C (host-side; advanced only when the call returns DG_OK).
+ * If q_new is not NULL, also computes the block's causal attention over the
+ * updated cache (query i at absolute position P+i sees keys 0..P+i):
+ *   out [C][Hq][hd] (dtype), lse [Hq][C] fp32 or NULL.
+ *   k_cache, v_cache [Hkv][cap][hd]   k_new, v_new [Hkv][C][hd]   q_new [C][Hq][hd]
+ * Requirements: *len + C <= cap; rows outside [*len, *len + C) are not written.
+ * Workspace: as dg_canvas_attn for (C, Hq, Hkv, hd, *len) when q_new != NULL.
+ */
+DG_API int dg_kv_append(void* k_cache, void* v_cache, int64_t cap, int64_t* len,
+                 const void* k_new, const void* v_new, int C, int Hkv, int hd, int dtype,
+                 const void* q_new, int Hq, void* out, float* lse,
+                 void* workspace, size_t workspace_bytes, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* DG_CANVAS_H */

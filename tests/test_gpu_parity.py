@@ -1,0 +1,250 @@
+"""GPU parity: every C-ABI call against the float64 oracle on the same seeded
+bytes. Sizes span several tiles and a ragged tail; the full-size workloads
+are checked on sampled rows."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from canvas_denoising_gb300 import binding as B
+from canvas_denoising_gb300 import synth
+from canvas_denoising_gb300.configs import WORKLOADS
+from tests.parity import (CONF_REL, FLAG_BUDGET, LSE_ABS, assert_rows_close, decision_flags, logit_gap_flags)
+
+pytestmark = pytest.mark.gpu
+
+
+def _np(t):
+    return t.detach().float().cpu().numpy() if t.dtype in (torch.bfloat16, torch.float16) else t.detach().cpu().numpy()
+
+
+def _status_ok():
+    assert B.device_status() == B.DG_OK
+
+
+# ------------------------------------------------------------------ re-noise / init (bit-exact)
+@pytest.mark.parametrize("C,V,thr,pos0", [(256, 262144, 0.3, 4096), (256, 32768, 0.5, 1024), (16, 512, 0.5, 32),
+                                          (1000, 1000, 0.5, 7), (256, 262144, 0.0, 0), (256, 262144, 1.0, 0)])
+def test_renoise_bit_exact(lib, C, V, thr, pos0):
+    g = torch.Generator().manual_seed(C + V)
+    am = torch.randint(0, V, (C,), generator=g, dtype=torch.int32)
+    conf = torch.rand(C, generator=g, dtype=torch.float32) * 0.999
+    conf[: min(8, C)] = thr  # equality is kept
+    tok = torch.full((C,), -1, dtype=torch.int32, device="cuda")
+    rn = torch.zeros(C, dtype=torch.uint8, device="cuda")
+    for step in (0, 5):
+        B.renoise(tok, am.cuda(), conf.cuda(), V, thr, 1234567, step, pos0, renoised=rn)
+        ref_tok, ref_rn = oracle.renoise(am.numpy(), conf.numpy(), V, thr, 1234567, step, pos0)
+        np.testing.assert_array_equal(_np(tok), ref_tok)
+        np.testing.assert_array_equal(_np(rn), ref_rn)
+    _status_ok()
+
+
+def test_canvas_init_bit_exact(lib):
+    for C, V, pos0, seed in ((256, 262144, 0, 0), (256, 262144, 2048 + 256 * 3, 5), (16, 512, 32, 0), (300, 999, 1, 9)):
+        tok = torch.empty(C, dtype=torch.int32, device="cuda")
+        B.canvas_init(tok, V, seed, pos0)
+        np.testing.assert_array_equal(_np(tok), oracle.canvas_init(C, V, seed, pos0))
+
+
+def test_renoise_out_of_range_argmax_latches_bounds(lib):
+    tok = torch.empty(4, dtype=torch.int32, device="cuda")
+    am = torch.tensor([1, 2, 70000, 3], dtype=torch.int32, device="cuda")
+    conf = torch.ones(4, dtype=torch.float32, device="cuda")
+    B.renoise(tok, am, conf, 1000, 0.5, 0, 0, 0)
+    assert B.device_status() == B.DG_ERR_DEVICE_BOUNDS
+    assert B.device_status() == B.DG_OK  # cleared by the read
+
+
+# ------------------------------------------------------------------ KV append
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+def test_kv_append_bytes_and_causal_attention(lib, dtype):
+    Hkv, Hq, hd, P, C, cap = 2, 4, 64, 37, 50, 160
+    k, v = synth.kv_prefix(Hkv, cap, hd, P, seed=3, dtype=dtype)
+    k[:, P + C:] = 7.0  # rows beyond the block must stay untouched
+    q, kn, vn = synth.canvas_qkv(C, Hq, Hkv, hd, seed=3, dtype=dtype)
+    kd, vd = k.cuda(), v.cuda()
+    n, out, lse = B.kv_append(kd, vd, P, kn.cuda(), vn.cuda(), q_new=q.cuda())
+    assert n == P + C
+    ref_k, ref_v, _ = oracle.kv_append(k.numpy() if dtype == torch.float32 else k.view(torch.int16).numpy(),
+                                       v.numpy() if dtype == torch.float32 else v.view(torch.int16).numpy(), P,
+                                       kn.numpy() if dtype == torch.float32 else kn.view(torch.int16).numpy(),
+                                       vn.numpy() if dtype == torch.float32 else vn.view(torch.int16).numpy())
+    got_k = kd.cpu() if dtype == torch.float32 else kd.cpu().view(torch.int16)
+    got_v = vd.cpu() if dtype == torch.float32 else vd.cpu().view(torch.int16)
+    assert got_k.numpy().tobytes() == ref_k.tobytes()
+    assert got_v.numpy().tobytes() == ref_v.tobytes()
+    ro, rl = oracle.canvas_attention(_np(q), _np(k), _np(v), P, _np(kn), _np(vn), causal=True)
+    assert_rows_close(_np(out).reshape(C * Hq, hd), ro.reshape(C * Hq, hd), what="causal out")
+    assert np.abs(_np(lse) - rl).max() <= LSE_ABS
+    _status_ok()
+
+
+def test_kv_append_rejects_overflow_without_touching(lib):
+    k = torch.zeros((1, 10, 32), dtype=torch.bfloat16, device="cuda")
+    v = torch.zeros_like(k)
+    kn = torch.ones((1, 4, 32), dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(B.DGError) as e:
+        B.kv_append(k, v, 7, kn, kn.clone())
+    assert e.value.code == B.DG_ERR_INVALID_ARG
+    assert float(k.abs().sum()) == 0.0
+
+
+# ------------------------------------------------------------------ attention
+@pytest.mark.parametrize("mask", [B.DG_MASK_BIDIR, B.DG_MASK_CAUSAL_BLOCK])
+@pytest.mark.parametrize("C,Hq,Hkv,hd,P", [(40, 4, 2, 128, 37), (256, 8, 4, 128, 1024), (16, 2, 1, 32, 32),
+                                           (77, 6, 3, 64, 0), (1, 2, 2, 128, 300), (130, 16, 8, 128, 700)])
+def test_canvas_attn_bf16(lib, mask, C, Hq, Hkv, hd, P):
+    cap = P + C + 5
+    k, v = synth.kv_prefix(Hkv, cap, hd, P, seed=11)
+    q, kn, vn = synth.canvas_qkv(C, Hq, Hkv, hd, seed=11, step=1)
+    out, lse = B.canvas_attn(q.cuda(), k.cuda(), v.cuda(), P, kn.cuda(), vn.cuda(), mask=mask)
+    ro, rl = oracle.canvas_attention(_np(q), _np(k), _np(v), P, _np(kn), _np(vn), causal=mask == 1)
+    assert_rows_close(_np(out).reshape(C * Hq, hd), ro.reshape(C * Hq, hd), what="attn out")
+    assert np.abs(_np(lse) - rl).max() <= LSE_ABS
+    _status_ok()
+
+
+def test_canvas_attn_f32_tiny(lib):
+    w = WORKLOADS["tiny_f32"]
+    k, v = synth.kv_prefix(w.Hkv, w.cap, w.hd, w.prefix, w.seed, dtype=torch.float32)
+    q, kn, vn = synth.canvas_qkv(w.C, w.Hq, w.Hkv, w.hd, w.seed, dtype=torch.float32)
+    for mask in (0, 1):
+        out, lse = B.canvas_attn(q.cuda(), k.cuda(), v.cuda(), w.prefix, kn.cuda(), vn.cuda(), mask=mask)
+        ro, rl = oracle.canvas_attention(_np(q), _np(k), _np(v), w.prefix, _np(kn), _np(vn), causal=mask == 1)
+        assert_rows_close(_np(out).reshape(-1, w.hd), ro.reshape(-1, w.hd), tol=1e-4)
+        assert np.abs(_np(lse) - rl).max() <= 1e-4
+
+
+def test_canvas_attn_permutation_equivariant(lib):
+    C, Hq, Hkv, hd, P = 64, 4, 2, 128, 200
+    k, v = synth.kv_prefix(Hkv, P + C, hd, P, seed=2)
+    q, kn, vn = synth.canvas_qkv(C, Hq, Hkv, hd, seed=2)
+    perm = torch.randperm(C, generator=torch.Generator().manual_seed(0))
+    o1, l1 = B.canvas_attn(q.cuda(), k.cuda(), v.cuda(), P, kn.cuda(), vn.cuda())
+    o2, l2 = B.canvas_attn(q[perm].contiguous().cuda(), k.cuda(), v.cuda(), P, kn[:, perm].contiguous().cuda(),
+                           vn[:, perm].contiguous().cuda())
+    assert_rows_close(_np(o2).reshape(C * Hq, hd), _np(o1)[perm.numpy()].reshape(C * Hq, hd), tol=1e-2)
+    assert np.abs(_np(l2) - _np(l1)[:, perm.numpy()]).max() < 1e-3
+
+
+# ------------------------------------------------------------------ vocabulary step
+def _vocab_case(C, V, d, seed=0, alpha=0.0, std=0.02, dtype=torch.bfloat16):
+    emb = synth.embedding(V, d, seed, dtype=dtype, std=std)
+    tgt = synth.targets(C, V, seed)
+    h = synth.hidden(emb, tgt, alpha, seed, dtype=dtype)
+    return h, emb
+
+
+def _check_vocab(h, emb, res, ref):
+    am, conf, lse, sc = (_np(x) for x in res)
+    flags = logit_gap_flags(ref)
+    ok = (am == ref["argmax"]) | flags
+    assert ok.all(), f"argmax mismatch at rows {np.nonzero(~ok)[0][:8]}"
+    np.testing.assert_allclose(conf, ref["conf"], rtol=CONF_REL)
+    assert np.abs(lse - ref["lse"]).max() <= LSE_ABS
+    assert_rows_close(sc, ref["selfcond"], what="selfcond")
+
+
+@pytest.mark.parametrize("C,V,d,alpha,std", [
+    (256, 1000, 128, 0.0, 0.3),       # ragged vocabulary tail, every tile a sample tile
+    (256, 40000, 256, 4.0, 0.1),      # hundreds of tiles, most past the sample
+    (200, 9000, 320, 2.0, 0.1),       # ragged rows and a narrow last d-slice
+    (77, 33333, 192, 3.0, 0.1),       # one row half
+    (256, 32768, 1024, 26.0, 0.02),   # the 32k-vocabulary workload's shapes
+    (1, 4096, 64, 0.0, 1.0),
+])
+def test_vocab_step_bf16(lib, C, V, d, alpha, std):
+    h, emb = _vocab_case(C, V, d, seed=C + V, alpha=alpha, std=std)
+    res = B.vocab_step(h.cuda(), emb.cuda())
+    ref = oracle.vocab_step(_np(h), _np(emb))
+    _check_vocab(h, emb, res, ref)
+    _status_ok()
+
+
+def test_vocab_step_bf16_repeatable(lib):
+    h, emb = _vocab_case(256, 20000, 256, seed=4, alpha=3.0, std=0.1)
+    hd, ed = h.cuda(), emb.cuda()
+    r1 = [x.clone() for x in B.vocab_step(hd, ed)]
+    r2 = B.vocab_step(hd, ed)
+    for a, b in zip(r1, r2):
+        assert torch.equal(a, b)
+
+
+def test_vocab_step_overflow_row_is_recomputed(lib):
+    """A row whose maximum logit lies far above every sampled logit takes the
+    exact recompute path and still matches the oracle."""
+    C, V, d = 128, 40000, 128
+    emb = synth.embedding(V, d, 1, std=1.0)
+    h = synth.normal((C, d), 1, "misc", std=0.5)
+    h[0] = (2.0 * emb[39000].float()).to(torch.bfloat16)   # logit ~ 256 in the last tiles
+    h[5] = (1.5 * emb[20001].float()).to(torch.bfloat16)
+    res = B.vocab_step(h.cuda(), emb.cuda())
+    ref = oracle.vocab_step(_np(h), _np(emb))
+    assert _np(res[0])[0] == 39000
+    _check_vocab(h, emb, res, ref)
+
+
+def test_vocab_step_f32_tiny(lib):
+    w = WORKLOADS["tiny_f32"]
+    h, emb = _vocab_case(w.C, w.V, w.d, seed=0, dtype=torch.float32)
+    res = B.vocab_step(h.cuda(), emb.cuda())
+    ref = oracle.vocab_step(_np(h), _np(emb))
+    am, conf, lse, sc = (_np(x) for x in res)
+    np.testing.assert_array_equal(am, ref["argmax"])
+    np.testing.assert_allclose(conf, ref["conf"], rtol=1e-4)
+    np.testing.assert_allclose(lse, ref["lse"], atol=1e-4)
+    assert_rows_close(sc, ref["selfcond"], tol=1e-4)
+
+
+@pytest.mark.parametrize("name", ["v262k_d2816_p4k"])
+def test_vocab_step_full_size_sampled_rows(lib, name):
+    """The headline workload, in the launch configuration the benchmark times;
+    the oracle checks a sample of rows."""
+    w = WORKLOADS[name]
+    emb = synth.embedding(w.V, w.d, w.seed, device="cuda")
+    tgt = synth.targets(w.C, w.V, w.seed, device="cuda")
+    h = synth.hidden(emb, tgt, w.alpha, w.seed, step=0)
+    res = B.vocab_step(h, emb)
+    _status_ok()
+    rows = np.array([0, 1, 77, 128, 200, 255])
+    emb_h = _np(emb)
+    ref = oracle.vocab_step(_np(h)[rows], emb_h)
+    got = [(_np(x)[rows] if x.dim() == 1 else _np(x)[rows]) for x in res]
+    _check_vocab(None, None, [torch.from_numpy(g) for g in got], ref)
+
+
+# ------------------------------------------------------------------ one whole step, teacher-forced
+@pytest.mark.parametrize("name", ["tiny_f32", "v32k_d1024_p1k"])
+def test_denoise_steps_match_oracle(lib, name):
+    w = WORKLOADS[name]
+    dt = torch.float32 if w.dtype == "f32" else torch.bfloat16
+    emb = synth.embedding(w.V, w.d, w.seed, dtype=dt)
+    tgt = synth.targets(w.C, w.V, w.seed)
+    k, v = synth.kv_prefix(w.Hkv, w.cap, w.hd, w.prefix, w.seed, dtype=dt)
+    emb_d, k_d, v_d = emb.cuda(), k.cuda(), v.cuda()
+    thr = w.thresholds[0]
+    tokens = torch.empty(w.C, dtype=torch.int32, device="cuda")
+    B.canvas_init(tokens, w.V, w.seed, w.prefix)
+    np.testing.assert_array_equal(_np(tokens), oracle.canvas_init(w.C, w.V, w.seed, w.prefix))
+    flagged = total = 0
+    for step in range(min(w.steps, 3)):
+        q, kn, vn = synth.canvas_qkv(w.C, w.Hq, w.Hkv, w.hd, w.seed, step=step, dtype=dt)
+        h = synth.hidden(emb, tgt, w.alpha, w.seed, step=step, dtype=dt)
+        out, lse = B.canvas_attn(q.cuda(), k_d, v_d, w.prefix, kn.cuda(), vn.cuda())
+        am, conf, vl, sc = B.vocab_step(h.cuda(), emb_d)
+        B.renoise(tokens, am, conf, w.V, thr, w.seed, step, w.prefix)
+        ro, rl = oracle.canvas_attention(_np(q), _np(k), _np(v), w.prefix, _np(kn), _np(vn))
+        tol = 1e-4 if dt == torch.float32 else 2e-2
+        assert_rows_close(_np(out).reshape(-1, w.hd), ro.reshape(-1, w.hd), tol=tol)
+        rv = oracle.vocab_step(_np(h), _np(emb))
+        ref_tok, _ = oracle.renoise(rv["argmax"], rv["conf"].astype(np.float32), w.V, thr, w.seed, step, w.prefix)
+        fl = decision_flags(rv, thr)
+        got = _np(tokens)
+        assert ((got == ref_tok) | fl).all()
+        flagged += int(fl.sum())
+        total += w.C
+        assert_rows_close(_np(sc), rv["selfcond"], tol=tol)
+    assert flagged <= FLAG_BUDGET * total, f"{flagged}/{total} flagged"
