@@ -16,6 +16,8 @@
 // tiles of 128 (for small shapes).
 #include <math.h>
 
+#include <mutex>
+
 #include "dg_common.cuh"
 
 namespace dg {
@@ -313,32 +315,6 @@ __global__ void __launch_bounds__(NW * 32) attn_fwd_bf16(AttnArgs a) {
   }
 }
 
-// Merge split partials: lse = log sum_s exp(lse_s); O = sum_s exp(lse_s - lse) O_s.
-// One warp per (position, head).
-template <typename OutT>
-__global__ void attn_combine(const float* __restrict__ part_o, const float* __restrict__ part_lse, OutT* out,
-                             float* lse, int C, int Hq, int HD, int splits) {
-  int64_t w = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-  int lane = threadIdx.x & 31;
-  if (w >= (int64_t)C * Hq) return;
-  int64_t i = w / Hq, h = w % Hq;
-  float mx = -INFINITY;
-  for (int s = 0; s < splits; ++s) mx = fmaxf(mx, part_lse[((int64_t)s * Hq + h) * C + i]);
-  float ref = mx == -INFINITY ? 0.f : mx;
-  float tot = 0.f;
-  for (int s = 0; s < splits; ++s) tot += expf(part_lse[((int64_t)s * Hq + h) * C + i] - ref);
-  float inv = tot > 0.f ? 1.f / tot : 0.f;
-  for (int c = lane; c < HD; c += 32) {
-    float acc = 0.f;
-    for (int s = 0; s < splits; ++s) {
-      float wgt = expf(part_lse[((int64_t)s * Hq + h) * C + i] - ref);
-      acc += wgt * part_o[(((int64_t)s * C + i) * Hq + h) * HD + c];
-    }
-    out[(i * Hq + h) * HD + c] = (OutT)(acc * inv);
-  }
-  if (lse && lane == 0) lse[h * C + i] = tot > 0.f ? ref + logf(tot) : -INFINITY;
-}
-
 // fp32 path: one CTA (128 threads) per (query i, head h).
 __global__ void attn_fwd_f32(const float* __restrict__ q, const float* __restrict__ kc, const float* __restrict__ vc,
                              const float* __restrict__ kn, const float* __restrict__ vn, float* __restrict__ out,
@@ -396,9 +372,49 @@ __global__ void attn_fwd_f32(const float* __restrict__ q, const float* __restric
 
 }  // namespace
 
+// Merge split partials: lse = log sum_s exp(lse_s); O = sum_s exp(lse_s - lse) O_s.
+// One warp per (position, head): the lanes first hold the split weights
+// (splits <= 64, two per lane), then each lane owns HD/32 output columns.
+template <typename OutT>
+__global__ void attn_combine(const float* __restrict__ part_o, const float* __restrict__ part_lse, OutT* out,
+                             float* lse, int C, int Hq, int HD, int splits) {
+  int64_t w = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  int lane = threadIdx.x & 31;
+  if (w >= (int64_t)C * Hq) return;
+  int64_t i = w / Hq, h = w % Hq;
+  float l0 = lane < splits ? part_lse[((int64_t)lane * Hq + h) * C + i] : -INFINITY;
+  float l1 = lane + 32 < splits ? part_lse[((int64_t)(lane + 32) * Hq + h) * C + i] : -INFINITY;
+  float mx = fmaxf(l0, l1);
+  for (int o = 16; o; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+  const float ref = mx == -INFINITY ? 0.f : mx;
+  float w0 = expf(l0 - ref), w1 = expf(l1 - ref);
+  float tot = w0 + w1;
+  for (int o = 16; o; o >>= 1) tot += __shfl_xor_sync(0xffffffffu, tot, o);
+  const float inv = tot > 0.f ? 1.f / tot : 0.f;
+  for (int c = lane; c < HD; c += 32) {
+    float acc = 0.f;
+    for (int s = 0; s < splits; ++s) {
+      const float wgt = __shfl_sync(0xffffffffu, s < 32 ? w0 : w1, s & 31);
+      acc += wgt * part_o[(((int64_t)s * C + i) * Hq + h) * HD + c];
+    }
+    out[(i * Hq + h) * HD + c] = (OutT)(acc * inv);
+  }
+  if (lse && lane == 0) lse[h * C + i] = tot > 0.f ? ref + logf(tot) : -INFINITY;
+}
+
+int attn_combine_launch(const float* part_o, const float* part_lse, __nv_bfloat16* out, float* lse, int C, int Hq,
+                        int HD, int splits, cudaStream_t s) {
+  const int64_t warps = (int64_t)C * Hq;
+  const unsigned blocks = (unsigned)((warps * 32 + 255) / 256);
+  attn_combine<__nv_bfloat16><<<blocks, 256, 0, s>>>(part_o, part_lse, out, lse, C, Hq, HD, splits);
+  DG_LAUNCH_CHECK();
+  return DG_OK;
+}
+
 size_t attn_workspace(int C, int Hq, int Hkv, int hd, int64_t P, int dtype) {
   if (dtype != DG_BF16 || C < 1 || Hkv < 1 || Hq % Hkv) return 0;
   Plan pl = make_plan(C, Hq, Hkv, P);
+  if (hd == 128) attn_tc_plan(C, Hq, Hkv, P, &pl.splits, nullptr);
   if (pl.splits <= 1) return 0;
   size_t o = (size_t)pl.splits * C * Hq * hd * sizeof(float);
   o = (o + 255) & ~(size_t)255;
@@ -418,6 +434,9 @@ int attn_launch(const void* q, const void* k_cache, const void* v_cache, int64_t
     DG_LAUNCH_CHECK();
     return DG_OK;
   }
+  if (hd == 128)
+    return attn_tc_launch(q, k_cache, v_cache, cap, P, k_canvas, v_canvas, out, lse, C, Hq, Hkv, scale, mask, ws,
+                          ws_bytes, s);
   Plan pl = make_plan(C, Hq, Hkv, P);
   AttnArgs a;
   a.q = (const __nv_bfloat16*)q;
@@ -449,27 +468,29 @@ int attn_launch(const void* q, const void* k_cache, const void* v_cache, int64_t
   const int64_t M = (int64_t)grp * C;
   dim3 grid((unsigned)((M + BM - 1) / BM), Hkv, pl.splits);
   size_t smem = (size_t)(BM + 4 * BN) * hd * sizeof(__nv_bfloat16);
+  static std::once_flag once;
+  static cudaError_t attr_err = cudaSuccess;
+  std::call_once(once, [] {
+    const int m32 = (BM + 4 * BN) * 32 * 2, m64 = (BM + 4 * BN) * 64 * 2, m128 = (BM + 4 * BN) * 128 * 2;
+    cudaError_t e1 = cudaFuncSetAttribute(attn_fwd_bf16<32>, cudaFuncAttributeMaxDynamicSharedMemorySize, m32);
+    cudaError_t e2 = cudaFuncSetAttribute(attn_fwd_bf16<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, m64);
+    cudaError_t e3 = cudaFuncSetAttribute(attn_fwd_bf16<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, m128);
+    attr_err = e1 != cudaSuccess ? e1 : (e2 != cudaSuccess ? e2 : e3);
+  });
+  DG_CUDA_TRY(attr_err);
   switch (hd) {
     case 32:
-      DG_CUDA_TRY(cudaFuncSetAttribute(attn_fwd_bf16<32>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
       attn_fwd_bf16<32><<<grid, NW * 32, smem, s>>>(a);
       break;
     case 64:
-      DG_CUDA_TRY(cudaFuncSetAttribute(attn_fwd_bf16<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
       attn_fwd_bf16<64><<<grid, NW * 32, smem, s>>>(a);
       break;
     default:
-      DG_CUDA_TRY(cudaFuncSetAttribute(attn_fwd_bf16<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
       attn_fwd_bf16<128><<<grid, NW * 32, smem, s>>>(a);
       break;
   }
   DG_LAUNCH_CHECK();
-  if (pl.splits > 1) {
-    int64_t warps = (int64_t)C * Hq;
-    unsigned blocks = (unsigned)((warps * 32 + 255) / 256);
-    attn_combine<__nv_bfloat16><<<blocks, 256, 0, s>>>(a.part_o, a.part_lse, a.out, lse, C, Hq, hd, pl.splits);
-    DG_LAUNCH_CHECK();
-  }
+  if (pl.splits > 1) return attn_combine_launch(a.part_o, a.part_lse, a.out, lse, C, Hq, hd, pl.splits, s);
   return DG_OK;
 }
 

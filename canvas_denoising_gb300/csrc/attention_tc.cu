@@ -1,0 +1,496 @@
+// Canvas attention on the 5th-generation tensor cores (tcgen05), bf16,
+// head_dim 128: bidirectional (denoising) and causal-block (incremental
+// prefill) grouped-query attention of the canvas over [cache prefix ; canvas].
+//
+// DiffusionGemma explainer, "Architecture: incremental prefill and
+// denoising": in denoising mode every canvas query sees every canvas token
+// and the KV cache; in prefill mode attention is causal.
+//
+// One CTA per (128 query rows, KV head, key split). The Hq/Hkv query heads of
+// one KV head are stacked (row = position * group + head-in-group), so a K/V
+// tile feeds all of them. Keys come in tiles of 128: first the cache rows
+// [0, P), then the canvas rows [0, C); tiles never straddle the two, and the
+// tensor maps' row extents are exactly P and C, so rows past the end read as
+// zeros. Per tile:
+//   S = Q K^T      tcgen05, into one of two TMEM buffers (128 columns each)
+//   softmax        4 warps, one query row per thread: row max, a per-row
+//                  reference kept fixed unless a tile's max exceeds it by
+//                  2^8 (then O and the row sum are rescaled through TMEM),
+//                  P = exp2(s - ref) in bf16 written to shared memory in the
+//                  128-byte-swizzled K-major operand layout
+//   O += P V       tcgen05, V read MN-major, O accumulated in TMEM.
+// S(j+1) is issued before PV(j), so the tensor core works while the softmax
+// warps do. Splits write fp32 partials (O, lse) merged by attn_combine.
+// Every wait is bounded (about two seconds); on expiry the CTA latches
+// DG_ERR_TIMEOUT, drains what it issued, frees TMEM and returns.
+#include <cudaTypedefs.h>
+#include <math.h>
+
+#include <mutex>
+
+#include "dg_common.cuh"
+#include "sm100.cuh"
+#include "tmap.h"
+
+namespace dg {
+
+namespace {
+
+using namespace sm100;
+
+constexpr int kHD = 128;
+constexpr int kBM = 128;
+constexpr int kBN = 128;
+constexpr int kThreads = 192;  // warp 0: TMA, warp 1: MMA, warps 2..5: softmax + epilogue
+constexpr uint32_t kChunk = 16384;  // [128 rows x 64 bf16] swizzled block
+constexpr uint32_t kTile = 2 * kChunk;
+// shared memory: Q | K[2] | V[2] | P[2]
+constexpr uint32_t kOffQ = 0, kOffK = kTile, kOffV = 3 * kTile, kOffP = 5 * kTile, kSmem = 7 * kTile;
+constexpr float kRescale = 8.f;  // log2 units
+constexpr float kLn2 = 0.6931471805599453f;
+constexpr long long kTimeoutCycles = 4000000000ll;
+
+struct TcArgs {
+  const __nv_bfloat16* q;
+  __nv_bfloat16* out;
+  float* lse;
+  float* part_o;
+  float* part_lse;
+  int C, Hq, Hkv, grp;
+  int64_t P;
+  int n_cache_tiles, n_tiles, tiles_per_split, splits;
+  float scale_log2;
+  int causal;
+  int* status;
+};
+
+struct Ctl {
+  volatile int* abort;
+  int* status;
+};
+
+__device__ bool wait_bar(uint32_t bar, uint32_t parity, const Ctl& c) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const long long t0 = clock64();
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((it & 255u) == 0) {
+      if (*c.abort) return false;
+      if (clock64() - t0 > kTimeoutCycles) {
+        *c.abort = 1;
+        latch(c.status, DG_ERR_TIMEOUT);
+        return false;
+      }
+    }
+  }
+}
+
+__device__ __forceinline__ bool sm_any(bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n .reg .pred pi, po;\n setp.ne.u32 pi, %1, 0;\n barrier.red.or.pred po, 1, 128, pi;\n"
+      " selp.u32 %0, 1, 0, po;\n}\n"
+      : "=r"(r)
+      : "r"((uint32_t)v)
+      : "memory");
+  return r != 0;
+}
+
+__device__ __forceinline__ int64_t min64(int64_t x, int64_t y) { return x < y ? x : y; }
+
+__device__ __forceinline__ uint32_t pack2(float a, float b) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    attn_fwd_tc(const __grid_constant__ CUtensorMap tk_c, const __grid_constant__ CUtensorMap tv_c,
+                const __grid_constant__ CUtensorMap tk_n, const __grid_constant__ CUtensorMap tv_n, const TcArgs a) {
+  extern __shared__ __align__(1024) uint8_t smem_dyn[];
+  __shared__ __align__(8) uint64_t k_full[2], k_empty[2], v_full[2], v_empty[2], s_full[2], s_empty[2], p_full[2],
+      p_empty[2], o_done, drain;
+  __shared__ uint32_t tmem_slot;
+  __shared__ int abort_flag;
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  uint8_t* sm = (uint8_t*)(((uintptr_t)smem_dyn + 1023) & ~(uintptr_t)1023);
+  const uint32_t sbase = smem_addr(sm);
+  const int mblk = blockIdx.x, g = blockIdx.y, split = blockIdx.z;
+  const int64_t M = (int64_t)a.grp * a.C;
+  Ctl ctl{&abort_flag, a.status};
+
+  // tiles of this CTA
+  int T0 = split * a.tiles_per_split;
+  int T1 = min(a.n_tiles, T0 + a.tiles_per_split);
+  if (a.causal) {
+    int64_t rmax = min64(M - 1, (int64_t)mblk * kBM + kBM - 1);
+    int64_t imax = rmax / a.grp;  // last visible key: P + imax (a canvas row)
+    int last = a.n_cache_tiles + (int)(imax / kBN);
+    T1 = min(T1, last + 1);
+  }
+  const int n = T1 > T0 ? T1 - T0 : 0;
+
+  if (tid == 0) {
+    abort_flag = 0;
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(smem_addr(&k_full[s]), 1);
+      mbar_init(smem_addr(&k_empty[s]), 1);
+      mbar_init(smem_addr(&v_full[s]), 1);
+      mbar_init(smem_addr(&v_empty[s]), 1);
+      mbar_init(smem_addr(&s_full[s]), 1);
+      mbar_init(smem_addr(&s_empty[s]), 128);
+      mbar_init(smem_addr(&p_full[s]), 128);
+      mbar_init(smem_addr(&p_empty[s]), 1);
+    }
+    mbar_init(smem_addr(&o_done), 1);
+    mbar_init(smem_addr(&drain), 1);
+    fence_mbar_init();
+    if (a.P > 0) {
+      prefetch_tmap(&tk_c);
+      prefetch_tmap(&tv_c);
+    }
+    prefetch_tmap(&tk_n);
+    prefetch_tmap(&tv_n);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_addr(&tmem_slot), 512);
+    tmem_relinquish();
+  }
+  // Q tile -> shared memory in the swizzled K-major layout (all threads)
+  for (int idx = tid; idx < kBM * 16; idx += kThreads) {
+    const int r = idx >> 4, ch = idx & 15;
+    const int64_t R = (int64_t)mblk * kBM + r;
+    const bool ok = R < M;
+    const int64_t i = ok ? R / a.grp : 0, j = ok ? R % a.grp : 0;
+    const __nv_bfloat16* src = a.q + ((i * a.Hq + (int64_t)g * a.grp + j) * kHD + ch * 8);
+    const uint32_t dst = sbase + kOffQ + (ch >> 3) * kChunk + r * 128 + ((((uint32_t)ch & 7u) ^ ((uint32_t)r & 7u)) << 4);
+    const int sz = ok ? 16 : 0;
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(dst), "l"(src), "r"(sz) : "memory");
+  }
+  asm volatile("cp.async.commit_group;\ncp.async.wait_group 0;\n" ::: "memory");
+  fence_proxy_async_smem();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_slot;
+  const uint32_t tS = tmem, tO = tmem + 256;
+
+  if (warp == 0) {
+    // ------------------------------------------------ TMA producer
+    if (lane == 0 && n > 0) {
+      bool issued_k[2] = {false, false}, issued_v[2] = {false, false};
+      uint32_t par_k[2] = {0, 0}, par_v[2] = {0, 0};
+      for (int jj = 0; jj < n; ++jj) {
+        const int t = T0 + jj, slot = jj & 1;
+        const uint32_t ph = (uint32_t)(jj >> 1) & 1u;
+        const bool cache = t < a.n_cache_tiles;
+        const int y = cache ? t * kBN : (t - a.n_cache_tiles) * kBN;
+        const CUtensorMap* mk = cache ? &tk_c : &tk_n;
+        const CUtensorMap* mv = cache ? &tv_c : &tv_n;
+        if (!wait_bar(smem_addr(&k_empty[slot]), ph ^ 1u, ctl)) break;
+        mbar_expect_tx(smem_addr(&k_full[slot]), kTile);
+        tma_load_3d(sbase + kOffK + slot * kTile, mk, 0, y, g, smem_addr(&k_full[slot]));
+        tma_load_3d(sbase + kOffK + slot * kTile + kChunk, mk, 64, y, g, smem_addr(&k_full[slot]));
+        issued_k[slot] = true;
+        par_k[slot] = ph;
+        if (!wait_bar(smem_addr(&v_empty[slot]), ph ^ 1u, ctl)) break;
+        mbar_expect_tx(smem_addr(&v_full[slot]), kTile);
+        tma_load_3d(sbase + kOffV + slot * kTile, mv, 0, y, g, smem_addr(&v_full[slot]));
+        tma_load_3d(sbase + kOffV + slot * kTile + kChunk, mv, 64, y, g, smem_addr(&v_full[slot]));
+        issued_v[slot] = true;
+        par_v[slot] = ph;
+      }
+      for (int s = 0; s < 2; ++s) {
+        if (issued_k[s]) wait_bar(smem_addr(&k_full[s]), par_k[s], ctl);
+        if (issued_v[s]) wait_bar(smem_addr(&v_full[s]), par_v[s], ctl);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------------------------ MMA issuer
+    if (lane == 0 && n > 0) {
+      const uint32_t id_s = idesc_bf16_f32(128, kBN, 0, 0);
+      const uint32_t id_o = idesc_bf16_f32(128, kHD, 0, 1);
+      auto issue_s = [&](int jj) -> bool {
+        const int slot = jj & 1;
+        const uint32_t ph = (uint32_t)(jj >> 1) & 1u;
+        if (!wait_bar(smem_addr(&k_full[slot]), ph, ctl)) return false;
+        if (!wait_bar(smem_addr(&s_empty[slot]), ph ^ 1u, ctl)) return false;
+        tc_fence_after();
+        const uint32_t kb = sbase + kOffK + slot * kTile;
+#pragma unroll
+        for (int kk = 0; kk < kHD / 16; ++kk) {
+          const uint64_t ad = sdesc_sw128(sbase + kOffQ + (kk >> 2) * kChunk + (kk & 3) * 32, 0, 1024);
+          const uint64_t bd = sdesc_sw128(kb + (kk >> 2) * kChunk + (kk & 3) * 32, 0, 1024);
+          mma_bf16(tS + slot * 128, ad, bd, id_s, kk > 0);
+        }
+        mma_commit(smem_addr(&k_empty[slot]));
+        mma_commit(smem_addr(&s_full[slot]));
+        return true;
+      };
+      bool ok = issue_s(0);
+      for (int jj = 0; jj < n && ok; ++jj) {
+        if (jj + 1 < n && !issue_s(jj + 1)) break;
+        const int slot = jj & 1;
+        const uint32_t ph = (uint32_t)(jj >> 1) & 1u;
+        if (!wait_bar(smem_addr(&p_full[slot]), ph, ctl)) break;
+        if (!wait_bar(smem_addr(&v_full[slot]), ph, ctl)) break;
+        tc_fence_after();
+        const uint32_t pb = sbase + kOffP + slot * kTile, vb = sbase + kOffV + slot * kTile;
+#pragma unroll
+        for (int kk = 0; kk < kBN / 16; ++kk) {
+          const uint64_t ad = sdesc_sw128(pb + (kk >> 2) * kChunk + (kk & 3) * 32, 0, 1024);
+          const uint64_t bd = sdesc_sw128(vb + kk * 2048, kChunk, 1024);
+          mma_bf16(tO, ad, bd, id_o, (jj > 0 || kk > 0) ? 1u : 0u);
+        }
+        mma_commit(smem_addr(&v_empty[slot]));
+        mma_commit(smem_addr(&p_empty[slot]));
+        mma_commit(smem_addr(&o_done));
+      }
+      mma_commit(smem_addr(&drain));
+      wait_bar(smem_addr(&drain), 0, ctl);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------ softmax + epilogue (one query row per thread)
+    const int q4 = warp & 3;
+    const int r = q4 * 32 + lane;
+    const uint32_t loff = (uint32_t)(q4 * 32) << 16;
+    const int64_t R = (int64_t)mblk * kBM + r;
+    const bool row_ok = R < M;
+    const int64_t i = row_ok ? R / a.grp : 0;
+    const int64_t h = (int64_t)g * a.grp + (row_ok ? R % a.grp : 0);
+    float ref = -INFINITY, l = 0.f;
+    bool ok = true;
+    int done_tiles = 0;
+    for (int jj = 0; jj < n; ++jj) {
+      const int t = T0 + jj, slot = jj & 1;
+      const uint32_t ph = (uint32_t)(jj >> 1) & 1u;
+      // visible columns of this tile for this row: [0, lim)
+      int lim;
+      if (t < a.n_cache_tiles) {
+        lim = (int)min64(kBN, a.P - (int64_t)t * kBN);
+      } else {
+        const int64_t c0 = (int64_t)(t - a.n_cache_tiles) * kBN;
+        lim = (int)min64(kBN, a.C - c0);
+        if (a.causal) lim = (int)min64(lim, i - c0 + 1);
+      }
+      if (!row_ok || lim < 0) lim = 0;
+      const bool got = wait_bar(smem_addr(&s_full[slot]), ph, ctl);
+      if (sm_any(!got)) { ok = false; break; }
+      tc_fence_after();
+      const uint32_t sa = tS + loff + slot * 128;
+      float v[kBN];
+      tmem_ld128(sa, v);  // the whole S row of this tile, one load, one wait
+      const bool full = lim == kBN;
+      if (!full) {
+#pragma unroll
+        for (int e = 0; e < kBN; ++e)
+          if (e >= lim) v[e] = -INFINITY;
+      }
+      float mx8[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) mx8[e] = v[e];
+#pragma unroll
+      for (int e = 8; e < kBN; ++e) mx8[e & 7] = fmaxf(mx8[e & 7], v[e]);
+      float mt = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                       fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+      mt *= a.scale_log2;  // scale > 0 keeps the order
+      bool need = false;
+      float factor = 1.f;
+      if (mt > -INFINITY) {
+        if (ref == -INFINITY) {
+          ref = mt;  // first visible keys of this row: O and l are still zero
+        } else if (mt > ref + kRescale) {
+          need = true;
+          factor = exp2f(ref - mt);
+          ref = mt;
+          l *= factor;
+        }
+      }
+      if (__any_sync(0xffffffffu, need)) {
+        // O must hold every PV issued so far before it is rescaled in place
+        const bool od = wait_bar(smem_addr(&o_done), (uint32_t)(jj - 1) & 1u, ctl);
+        if (!__all_sync(0xffffffffu, od)) { ok = false; }
+        tc_fence_after();
+        if (ok) {
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            float o[32];
+            tmem_ld32(tO + loff + c * 32, o);
+#pragma unroll
+            for (int e = 0; e < 32; ++e) o[e] *= factor;
+            tmem_st32(tO + loff + c * 32, o);
+          }
+        }
+      }
+      if (sm_any(!ok)) { ok = false; break; }
+      const bool pe = wait_bar(smem_addr(&p_empty[slot]), ph ^ 1u, ctl);
+      if (sm_any(!pe)) { ok = false; break; }
+      uint8_t* prow = sm + kOffP + slot * kTile + r * 128;
+      const float rr = ref == -INFINITY ? 0.f : ref;
+      float sum8[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) sum8[e] = 0.f;
+#pragma unroll
+      for (int c = 0; c < kBN / 8; ++c) {
+        // 8 keys -> one 16-byte piece of the swizzled P row
+        float p8[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          p8[e] = ex2_approx(fmaf(v[c * 8 + e], a.scale_log2, -rr));  // exp2(-inf) = 0 for masked keys
+          sum8[e] += p8[e];
+        }
+        const int chunk = c >> 3, piece = c & 7;
+        *reinterpret_cast<uint4*>(prow + chunk * kChunk + ((piece ^ (r & 7)) << 4)) =
+            make_uint4(pack2(p8[0], p8[1]), pack2(p8[2], p8[3]), pack2(p8[4], p8[5]), pack2(p8[6], p8[7]));
+      }
+      l += ((sum8[0] + sum8[1]) + (sum8[2] + sum8[3])) + ((sum8[4] + sum8[5]) + (sum8[6] + sum8[7]));
+      tc_fence_before();
+      mbar_arrive(smem_addr(&s_empty[slot]));
+      fence_proxy_async_smem();
+      mbar_arrive(smem_addr(&p_full[slot]));
+      done_tiles = jj + 1;
+    }
+    // epilogue
+    bool have = ok && done_tiles == n && n > 0;
+    if (have) {
+      const bool od = wait_bar(smem_addr(&o_done), (uint32_t)(n - 1) & 1u, ctl);
+      have = !sm_any(!od);
+      tc_fence_after();
+    }
+    const float inv = l > 0.f ? 1.f / l : 0.f;
+    const float lse_v = l > 0.f ? (ref + log2f(l)) * kLn2 : -INFINITY;
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      float v[32];
+      if (have) {
+        tmem_ld32(tO + loff + c * 32, v);
+      } else {
+#pragma unroll
+        for (int e = 0; e < 32; ++e) v[e] = 0.f;
+      }
+      if (!row_ok) continue;
+      if (a.splits == 1) {
+        __nv_bfloat16* dst = a.out + (i * a.Hq + h) * kHD + c * 32;
+#pragma unroll
+        for (int e = 0; e < 32; e += 8) {
+          uint4 w = make_uint4(pack2(v[e] * inv, v[e + 1] * inv), pack2(v[e + 2] * inv, v[e + 3] * inv),
+                               pack2(v[e + 4] * inv, v[e + 5] * inv), pack2(v[e + 6] * inv, v[e + 7] * inv));
+          *reinterpret_cast<uint4*>(dst + e) = w;
+        }
+      } else {
+        float* dst = a.part_o + (((int64_t)split * a.C + i) * a.Hq + h) * kHD + c * 32;
+#pragma unroll
+        for (int e = 0; e < 32; e += 4)
+          *reinterpret_cast<float4*>(dst + e) = make_float4(v[e] * inv, v[e + 1] * inv, v[e + 2] * inv, v[e + 3] * inv);
+      }
+    }
+    if (row_ok) {
+      if (a.splits == 1) {
+        if (a.lse) a.lse[h * a.C + i] = lse_v;
+      } else {
+        a.part_lse[((int64_t)split * a.Hq + h) * a.C + i] = lse_v;
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+// [heads][rows][128] bf16 with `rows_alloc` rows per head in memory and
+// `rows` valid ones; box [1][128 rows][64 columns], 128-byte swizzle.
+bool make_kv_map(CUtensorMap* m, const void* base, int64_t rows, int64_t rows_alloc, int heads) {
+  const uint64_t dims[3] = {(uint64_t)kHD, (uint64_t)rows, (uint64_t)heads};
+  const uint64_t strides[2] = {(uint64_t)kHD * 2, (uint64_t)rows_alloc * kHD * 2};
+  const uint32_t box[3] = {64, (uint32_t)kBN, 1};
+  return tmap_bf16_sw128(m, base, 3, dims, strides, box);
+}
+
+int num_sms() {
+  static int n = 0;
+  if (!n) {
+    int dev = 0, v = 0;
+    if (cudaGetDevice(&dev) == cudaSuccess &&
+        cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && v > 0)
+      n = v;
+    else
+      n = 152;
+  }
+  return n;
+}
+
+}  // namespace
+
+// Split plan of the tensor-core path: one wave of CTAs (one per SM).
+void attn_tc_plan(int C, int Hq, int Hkv, int64_t P, int* splits, int* tiles_per_split) {
+  const int64_t M = (int64_t)(Hq / Hkv) * C;
+  const int64_t base = ((M + kBM - 1) / kBM) * Hkv;
+  const int nct = (int)((P + kBN - 1) / kBN), nvt = (C + kBN - 1) / kBN;
+  const int tiles = nct + nvt;
+  int want = (int)(num_sms() / base);
+  if (want < 1) want = 1;
+  if (want > tiles) want = tiles;
+  if (want > 64) want = 64;
+  const int tps = (tiles + want - 1) / want;
+  if (tiles_per_split) *tiles_per_split = tps;
+  *splits = (tiles + tps - 1) / tps;
+}
+
+int attn_tc_launch(const void* q, const void* k_cache, const void* v_cache, int64_t cap, int64_t P,
+                   const void* k_canvas, const void* v_canvas, void* out, float* lse, int C, int Hq, int Hkv,
+                   float scale, int mask, void* ws, size_t ws_bytes, cudaStream_t s) {
+  int splits, tps;
+  attn_tc_plan(C, Hq, Hkv, P, &splits, &tps);
+  int* st = status_ptr();
+  if (!st) return DG_ERR_CUDA;
+  CUtensorMap tk_c, tv_c, tk_n, tv_n;
+  memset(&tk_c, 0, sizeof(tk_c));
+  memset(&tv_c, 0, sizeof(tv_c));
+  if (P > 0 && (!make_kv_map(&tk_c, k_cache, P, cap, Hkv) || !make_kv_map(&tv_c, v_cache, P, cap, Hkv)))
+    return DG_ERR_CUDA;
+  if (!make_kv_map(&tk_n, k_canvas, C, C, Hkv) || !make_kv_map(&tv_n, v_canvas, C, C, Hkv)) return DG_ERR_CUDA;
+  TcArgs a;
+  a.q = (const __nv_bfloat16*)q;
+  a.out = (__nv_bfloat16*)out;
+  a.lse = lse;
+  a.C = C;
+  a.Hq = Hq;
+  a.Hkv = Hkv;
+  a.grp = Hq / Hkv;
+  a.P = P;
+  a.n_cache_tiles = (int)((P + kBN - 1) / kBN);
+  a.n_tiles = a.n_cache_tiles + (C + kBN - 1) / kBN;
+  a.tiles_per_split = tps;
+  a.splits = splits;
+  a.scale_log2 = scale * 1.4426950408889634f;
+  a.causal = mask == DG_MASK_CAUSAL_BLOCK;
+  a.status = st;
+  a.part_o = nullptr;
+  a.part_lse = nullptr;
+  if (splits > 1) {
+    size_t o = (size_t)splits * C * Hq * kHD * sizeof(float);
+    o = (o + 255) & ~(size_t)255;
+    if (ws_bytes < o + (size_t)splits * Hq * C * sizeof(float)) return DG_ERR_WORKSPACE;
+    a.part_o = (float*)ws;
+    a.part_lse = (float*)((char*)ws + o);
+  }
+  static std::once_flag once;
+  static cudaError_t attr_err = cudaSuccess;
+  std::call_once(once, [] {
+    attr_err = cudaFuncSetAttribute(attn_fwd_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmem + 1024);
+  });
+  DG_CUDA_TRY(attr_err);
+  const int64_t M = (int64_t)a.grp * C;
+  dim3 grid((unsigned)((M + kBM - 1) / kBM), Hkv, splits);
+  attn_fwd_tc<<<grid, kThreads, kSmem + 1024, s>>>(tk_c, tv_c, tk_n, tv_n, a);
+  DG_LAUNCH_CHECK();
+  if (splits > 1) return attn_combine_launch(a.part_o, a.part_lse, a.out, lse, C, Hq, kHD, splits, s);
+  return DG_OK;
+}
+
+}  // namespace dg

@@ -68,6 +68,12 @@ int attn_launch(const void* q, const void* k_cache, const void* v_cache, int64_t
                 const void* k_canvas, const void* v_canvas, void* out, float* lse, int C, int Hq, int Hkv,
                 int hd, float scale, int dtype, int mask, void* ws, size_t ws_bytes, cudaStream_t s);
 size_t attn_workspace(int C, int Hq, int Hkv, int hd, int64_t P, int dtype);
+int attn_combine_launch(const float* part_o, const float* part_lse, __nv_bfloat16* out, float* lse, int C, int Hq,
+                        int HD, int splits, cudaStream_t s);
+void attn_tc_plan(int C, int Hq, int Hkv, int64_t P, int* splits, int* tiles_per_split);
+int attn_tc_launch(const void* q, const void* k_cache, const void* v_cache, int64_t cap, int64_t P,
+                   const void* k_canvas, const void* v_canvas, void* out, float* lse, int C, int Hq, int Hkv,
+                   float scale, int mask, void* ws, size_t ws_bytes, cudaStream_t s);
 
 int vocab_simt_launch(const float* h, const float* emb, int C, int V, int d, int32_t* argmax, float* conf,
                       float* lse, float* selfcond, cudaStream_t s);

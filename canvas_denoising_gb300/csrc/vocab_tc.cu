@@ -37,31 +37,45 @@
 // copies and MMAs, frees TMEM and returns.
 #include <cudaTypedefs.h>
 #include <math.h>
+#include <stdlib.h>
 
 #include <mutex>
 
 #include "dg_common.cuh"
 #include "sm100.cuh"
+#include "tmap.h"
 
 namespace dg {
 namespace {
 
 using namespace sm100;
 
-constexpr int kStages = 4;
+constexpr int kStages = 3;
 constexpr int kBK = 64;            // d elements per producer k-step (one 128-byte swizzle row)
-constexpr int kVT = 128;           // vocabulary ids per tile
+constexpr int kVT = 256;           // vocabulary ids per tile
 constexpr int kDT = 256;           // S columns per consumer CTA
-constexpr int kThreads = 192;      // warp 0: TMA, warp 1: MMA, warps 2..5: epilogue
-constexpr uint32_t kStageBytes = 48u * 1024u;
+constexpr int kThreads = 320;      // warp 0: TMA, warp 1: MMA, warps 2..9: epilogue
+constexpr int kEpiThreads = 256;
+constexpr uint32_t kStageBytes = 64u * 1024u;
+constexpr uint32_t kEBytesA = 32768u;  // producer E block [256 ids x 64 d]
 constexpr uint32_t kTileBytes = 16384u;  // [128 rows x 64 bf16], one swizzled operand block
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kTau = 40.f;       // overflow margin above the reference, natural log
 constexpr long long kTimeoutCycles = 4000000000ll;
+constexpr int kPrefetch = 0;       // producer k-steps of E prefetched into L2 ahead (measured: 12 was slower)
 
 struct Plan {
-  int n_rh, n_dt, n_vt, ksplit, n_a, n_c;
+  int n_rh, n_dt, n_vt, ksplit, n_a, n_c, window;
 };
+
+// Optional integer override from the environment (tuning knobs, read once).
+int env_int(const char* name, int dflt) {
+  const char* v = getenv(name);
+  if (!v || !*v) return dflt;
+  char* end = nullptr;
+  long x = strtol(v, &end, 10);
+  return (end && *end == 0 && x > 0 && x < (1 << 30)) ? (int)x : dflt;
+}
 
 int num_sms() {
   static int n = 0;
@@ -82,8 +96,9 @@ Plan make_plan(int C, int V, int d) {
   p.n_dt = (d + kDT - 1) / kDT;
   p.n_vt = (V + kVT - 1) / kVT;
   const int sms = num_sms();
-  const int tiles_c = p.n_rh * p.n_dt;
-  int ks = (int)lround((double)(sms / 2) / tiles_c);
+  const int tiles_c = p.n_dt;  // a consumer CTA covers every row for its d-slice
+  static const int ks_env = env_int("DG_VOCAB_KSPLIT", 0);
+  int ks = ks_env ? ks_env : (int)lround((double)(sms / 2) / tiles_c);
   if (ks < 1) ks = 1;
   if (ks > p.n_vt) ks = p.n_vt;
   while (ks > 1 && tiles_c * ks > sms - 1) --ks;
@@ -92,6 +107,17 @@ Plan make_plan(int C, int V, int d) {
   p.n_a = sms - p.n_c;
   if (p.n_a > p.n_vt) p.n_a = p.n_vt;
   if (p.n_a < 1) p.n_a = 1;
+  // Producers may run at most `window` tiles ahead of the slowest consumer, so
+  // that the E rows a consumer reads are still in L2 (about 80 MB of E in flight).
+  static const int win_env = env_int("DG_VOCAB_WINDOW", 0);
+  const double tile_bytes = (double)kVT * d * 2;
+  int win = (int)(80e6 / tile_bytes);
+  if (win > 2 * p.n_a) win = 2 * p.n_a;
+  if (win < p.n_a + 16) win = p.n_a + 16;
+  // Measured: coupling producers to the slowest consumer costs more than the
+  // re-reads it saves, so the window is off unless DG_VOCAB_WINDOW sets one.
+  (void)win;
+  p.window = win_env ? (win_env > p.n_a ? win_env : p.n_a + 1) : (1 << 30);
   return p;
 }
 
@@ -106,30 +132,31 @@ Layout make_layout(const Plan& p, int d) {
   Layout L;
   size_t o = 0;
   L.flags = o;
-  L.flag_bytes = (size_t)(p.n_vt + 2 + 256) * sizeof(int);
+  L.flag_bytes = (size_t)(2 * p.n_vt + 2 + 256) * sizeof(int);
   o += up256(L.flag_bytes);
   L.smax = o; o += up256((size_t)p.n_a * 256 * 4);
   L.am = o;   o += up256((size_t)p.n_a * 256 * 4);
   L.aa = o;   o += up256((size_t)p.n_a * 256 * 4);
   L.az = o;   o += up256((size_t)p.n_a * 256 * 4);
   L.cpart = o; o += up256((size_t)p.ksplit * 256 * d * 4);
-  L.pbuf = o; o += (size_t)p.n_vt * p.n_rh * 2 * kTileBytes;
+  L.pbuf = o; o += (size_t)p.n_vt * 4 * p.n_rh * kTileBytes;
   L.total = o;
   return L;
 }
 
 struct Params {
-  int C, V, d, n_rh, n_dt, n_vt, ksplit, n_a;
+  int C, V, d, n_rh, n_dt, n_vt, ksplit, n_a, window;
   int* ready;      // [n_vt] tile published counters
+  int* consumed;   // [n_vt] consumer CTAs that have fetched the tile
   int* ref_count;  // producers that have published their sample maxima
   int* abort_flag;
   int* overflow;   // [256]
-  float* smax;     // [n_a][256] sample maxima
-  float* am;       // [n_a][256] running max
-  int* aa;         // [n_a][256] first argmax
-  float* az;       // [n_a][256] sum of exp(l - R)
+  float* smax;     // [256][n_a] sample maxima
+  float* am;       // [256][n_a] running max
+  int* aa;         // [256][n_a] first argmax
+  float* az;       // [256][n_a] sum of exp(l - R)
   float* cpart;    // [ksplit][256][d]
-  uint8_t* pbuf;   // [n_vt][n_rh][2][16 KB]
+  uint8_t* pbuf;   // [n_vt][4 sub-tiles of 64 ids][n_rh][16 KB]
   int* status;
 };
 
@@ -170,14 +197,14 @@ __device__ bool wait_flag(const int* flag, int target, const Params& p) {
   }
 }
 
-__device__ __forceinline__ void epi_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+__device__ __forceinline__ void epi_sync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
 
-// Barrier over the 128 epilogue threads that also ORs a predicate across them,
+// Barrier over the 256 epilogue threads that also ORs a predicate across them,
 // so that every epilogue thread takes the same branch after a bounded wait.
 __device__ __forceinline__ bool epi_any(bool v) {
   uint32_t r;
   asm volatile(
-      "{\n .reg .pred pi, po;\n setp.ne.u32 pi, %1, 0;\n barrier.red.or.pred po, 1, 128, pi;\n"
+      "{\n .reg .pred pi, po;\n setp.ne.u32 pi, %1, 0;\n barrier.red.or.pred po, 1, 256, pi;\n"
       " selp.u32 %0, 1, 0, po;\n}\n"
       : "=r"(r)
       : "r"((uint32_t)v)
@@ -194,7 +221,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     vocab_main(const __grid_constant__ CUtensorMap tm_h, const __grid_constant__ CUtensorMap tm_ek,
                const __grid_constant__ CUtensorMap tm_emn, const Params p) {
   extern __shared__ __align__(1024) uint8_t smem_dyn[];
-  __shared__ __align__(8) uint64_t bar_full[kStages], bar_empty[kStages], bar_tfull[2], bar_tempty[2], bar_drain;
+  __shared__ __align__(8) uint64_t bar_full[kStages], bar_empty[kStages], bar_tfull, bar_tempty, bar_drain;
   __shared__ uint32_t tmem_slot;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -207,10 +234,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(smem_addr(&bar_full[s]), 1);
       mbar_init(smem_addr(&bar_empty[s]), 1);
     }
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(smem_addr(&bar_tfull[b]), 1);
-      mbar_init(smem_addr(&bar_tempty[b]), 128);
-    }
+    mbar_init(smem_addr(&bar_tfull), 1);
+    mbar_init(smem_addr(&bar_tempty), kEpiThreads);
     mbar_init(smem_addr(&bar_drain), 1);
     fence_mbar_init();
     prefetch_tmap(&tm_h);
@@ -238,10 +263,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t issued_par[kStages];
         bool issued[kStages];
         for (int s = 0; s < kStages; ++s) issued[s] = false, issued_par[s] = 0;
-        const uint32_t tx = (uint32_t)(p.n_rh + 1) * kTileBytes;
+        const uint32_t tx = (uint32_t)p.n_rh * kTileBytes + kEBytesA;
+        const int n_cons = p.n_dt;  // consumer CTAs per tile
         bool ok = true;
         for (int j = 0; j < n_my && ok; ++j) {
           const int t = a + j * p.n_a;
+          if (t >= p.window && !wait_flag(p.consumed + (t - p.window), n_cons, p)) break;
           for (int ks = 0; ks < ksteps_d; ++ks) {
             if (!wait_bar(smem_addr(&bar_empty[stage]), ph ^ 1, p)) { ok = false; break; }
             const uint32_t fb = smem_addr(&bar_full[stage]);
@@ -254,7 +281,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (++stage == kStages) { stage = 0; ph ^= 1; }
           }
         }
-        // drain: every copy this thread issued has landed before the CTA may exit
         for (int s = 0; s < kStages; ++s)
           if (issued[s]) wait_bar(smem_addr(&bar_full[s]), issued_par[s], p);
       }
@@ -266,9 +292,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t ph = 0;
         bool ok = true;
         for (int j = 0; j < n_my && ok; ++j) {
-          const int b = j & 1;
-          const uint32_t u = (uint32_t)(j >> 1);
-          if (!wait_bar(smem_addr(&bar_tempty[b]), (u & 1) ^ 1, p)) break;
+          // single accumulator: the epilogue must have drained the previous tile
+          if (!wait_bar(smem_addr(&bar_tempty), (uint32_t)(j & 1) ^ 1u, p)) break;
           tc_fence_after();
           for (int ks = 0; ks < ksteps_d; ++ks) {
             if (!wait_bar(smem_addr(&bar_full[stage]), ph, p)) { ok = false; break; }
@@ -279,127 +304,132 @@ __global__ void __launch_bounds__(kThreads, 1)
               const uint64_t bdesc = sdesc_sw128(sb + 2 * kTileBytes + k * 32, 0, 1024);
               for (int h = 0; h < p.n_rh; ++h) {
                 const uint64_t adesc = sdesc_sw128(sb + h * kTileBytes + k * 32, 0, 1024);
-                mma_bf16(tmem + b * 256 + h * 128, adesc, bdesc, idesc, (ks | k) != 0);
+                mma_bf16(tmem + h * 256, adesc, bdesc, idesc, (ks | k) != 0);
               }
             }
             mma_commit(smem_addr(&bar_empty[stage]));
             if (++stage == kStages) { stage = 0; ph ^= 1; }
           }
-          if (ok) mma_commit(smem_addr(&bar_tfull[b]));
+          if (ok) mma_commit(smem_addr(&bar_tfull));
         }
         mma_commit(smem_addr(&bar_drain));
         wait_bar(smem_addr(&bar_drain), 0, p);
       }
       __syncwarp();
     } else {
-      // epilogue warps 2..5: TMEM lane quarter q = warp % 4, one row per thread per row half
+      // epilogue warps 2..9: row half hh = (warp-2)/4, TMEM lane quarter q = warp % 4
+      const int hh = (warp - 2) >> 2;
       const int q = warp & 3;
       const int r = q * 32 + lane;
-      const uint32_t lane_off = (uint32_t)(q * 32) << 16;
-      float R2[2] = {0.f, 0.f}, Rn[2] = {0.f, 0.f};
-      float m_run[2] = {-INFINITY, -INFINITY}, z_run[2] = {0.f, 0.f};
-      int a_run[2] = {0x7fffffff, 0x7fffffff};
-      bool ovf[2] = {false, false};
+      const int i = hh * 128 + r;
+      const bool active = hh < p.n_rh;
+      const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + hh * 256;
+      float R2 = 0.f, lim2 = 0.f;
+      float m_run = -INFINITY, z_run = 0.f;
+      int a_run = 0x7fffffff;
+      bool ovf = false;
       bool ok = true;
       if (n_my == 0) {
-        for (int h = 0; h < 2; ++h) p.smax[(size_t)a * 256 + h * 128 + r] = -INFINITY;
+        p.smax[(size_t)i * p.n_a + a] = -INFINITY;
         __threadfence();
         epi_sync();
         if (threadIdx.x == 64) red_release_add_gpu(p.ref_count, 1);
       }
       for (int j = 0; j < n_my && ok; ++j) {
-        const int b = j & 1;
-        const uint32_t u = (uint32_t)(j >> 1);
         const int t = a + j * p.n_a;
-        const bool got = wait_bar(smem_addr(&bar_tfull[b]), u & 1, p);
+        const bool got = wait_bar(smem_addr(&bar_tfull), (uint32_t)j & 1u, p);
         if (epi_any(!got)) { ok = false; break; }
         tc_fence_after();
         if (j == 0) {
           // sample maxima of this CTA's first tile -> grid-wide reference
-          for (int h = 0; h < 2; ++h) {
-            float mx = -INFINITY;
-            if (h < p.n_rh) {
-              for (int c = 0; c < kVT / 32; ++c) {
-                float v[32];
-                tmem_ld32(tmem + lane_off + b * 256 + h * 128 + c * 32, v);
+          float mx = -INFINITY;
+          if (active) {
+            for (int c = 0; c < kVT / 128; ++c) {
+              float v[128];
+              tmem_ld128(taddr + c * 128, v);
+              const int vb = t * kVT + c * 128;
 #pragma unroll
-                for (int e = 0; e < 32; ++e)
-                  if (t * kVT + c * 32 + e < p.V) mx = fmaxf(mx, v[e]);
-              }
+              for (int e = 0; e < 128; ++e)
+                if (vb + e < p.V) mx = fmaxf(mx, v[e]);
             }
-            p.smax[(size_t)a * 256 + h * 128 + r] = mx;
           }
+          p.smax[(size_t)i * p.n_a + a] = mx;
           __threadfence();
           epi_sync();
           if (threadIdx.x == 64) red_release_add_gpu(p.ref_count, 1);
           const bool refd = wait_flag(p.ref_count, p.n_a, p);
           if (epi_any(!refd)) { ok = false; break; }
-          for (int h = 0; h < 2; ++h) {
-            float R = -INFINITY;
-            for (int aa = 0; aa < p.n_a; ++aa) R = fmaxf(R, __ldcg(p.smax + (size_t)aa * 256 + h * 128 + r));
-            Rn[h] = R;
-            R2[h] = R * kLog2e;
-          }
+          float R = -INFINITY;
+          const float* sm_row = p.smax + (size_t)i * p.n_a;
+          for (int aa = 0; aa < p.n_a; ++aa) R = fmaxf(R, __ldcg(sm_row + aa));
+          R2 = R * kLog2e;
+          lim2 = (R + kTau) * kLog2e;
         }
-        for (int h = 0; h < p.n_rh; ++h) {
-          const float lim2 = (Rn[h] + kTau) * kLog2e;
-          for (int c = 0; c < kVT / 32; ++c) {
-            float v[32];
-            tmem_ld32(tmem + lane_off + b * 256 + h * 128 + c * 32, v);
-            const int vbase = t * kVT + c * 32;
-            uint32_t pk[16];
+        if (active) {
+          for (int c = 0; c < kVT / 128; ++c) {
+            float v[128];
+            tmem_ld128(taddr + c * 128, v);
+            const int vb = t * kVT + c * 128;
+            if (vb + 128 > p.V) {
 #pragma unroll
-            for (int e = 0; e < 32; e += 2) {
-              float pe[2];
+              for (int e = 0; e < 128; ++e)
+                if (vb + e >= p.V) v[e] = -INFINITY;
+            }
+            // running max / first argmax with 8 independent lanes of accumulators
+            float bm[8];
+            int bi[8];
 #pragma unroll
-              for (int f = 0; f < 2; ++f) {
-                const float l = v[e + f];
-                const int id = vbase + e + f;
-                float pv = 0.f;
-                if (id < p.V) {
-                  if (l > m_run[h]) { m_run[h] = l; a_run[h] = id; }
-                  const float x2 = l * kLog2e;
-                  if (x2 > lim2) ovf[h] = true;
-                  pv = exp2f(x2 - R2[h]);
-                  z_run[h] += pv;
-                }
-                pe[f] = pv;
+            for (int e = 0; e < 8; ++e) { bm[e] = v[e]; bi[e] = e; }
+#pragma unroll
+            for (int e = 8; e < 128; ++e)
+              if (v[e] > bm[e & 7]) { bm[e & 7] = v[e]; bi[e & 7] = e; }
+            float cm = bm[0];
+            int ci = bi[0];
+#pragma unroll
+            for (int e = 1; e < 8; ++e)
+              if (bm[e] > cm || (bm[e] == cm && bi[e] < ci)) { cm = bm[e]; ci = bi[e]; }
+            if (cm > m_run) { m_run = cm; a_run = vb + ci; }
+            if (cm * kLog2e > lim2) ovf = true;
+            float zs[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) zs[e] = 0.f;
+            uint8_t* prow = p.pbuf + ((size_t)((t * 4 + c * 2) * p.n_rh + hh)) * kTileBytes + (size_t)r * 128;
+#pragma unroll
+            for (int e8 = 0; e8 < 16; ++e8) {
+              float pe[8];
+#pragma unroll
+              for (int f = 0; f < 8; ++f) {
+                pe[f] = ex2_approx(fmaf(v[e8 * 8 + f], kLog2e, -R2));  // masked ids: exp2(-inf) = 0
+                zs[f] += pe[f];
               }
-              pk[e >> 1] = pack2(pe[0], pe[1]);
+              const int sub = e8 >> 3, piece = e8 & 7;
+              uint8_t* dst = prow + (size_t)sub * p.n_rh * kTileBytes + ((piece ^ (r & 7)) << 4);
+              *reinterpret_cast<uint4*>(dst) =
+                  make_uint4(pack2(pe[0], pe[1]), pack2(pe[2], pe[3]), pack2(pe[4], pe[5]), pack2(pe[6], pe[7]));
             }
-            uint8_t* dst = p.pbuf + ((size_t)(t * p.n_rh + h) * 2 + (c >> 1)) * kTileBytes + (size_t)r * 128;
-#pragma unroll
-            for (int jj = 0; jj < 4; ++jj) {
-              const int chunk = (c & 1) * 4 + jj;
-              uint4 w = make_uint4(pk[jj * 4 + 0], pk[jj * 4 + 1], pk[jj * 4 + 2], pk[jj * 4 + 3]);
-              *reinterpret_cast<uint4*>(dst + ((chunk ^ (r & 7)) << 4)) = w;
-            }
+            z_run += ((zs[0] + zs[1]) + (zs[2] + zs[3])) + ((zs[4] + zs[5]) + (zs[6] + zs[7]));
           }
         }
         tc_fence_before();
-        mbar_arrive(smem_addr(&bar_tempty[b]));
+        mbar_arrive(smem_addr(&bar_tempty));
         // publish the P tile to consumer CTAs (generic writes -> async-proxy reads elsewhere)
         fence_proxy_async_global();
         __threadfence();
         epi_sync();
         if (threadIdx.x == 64) red_release_add_gpu(p.ready + t, 1);
       }
-      for (int h = 0; h < p.n_rh; ++h) {
-        const int i = h * 128 + r;
-        if (i < p.C) {
-          p.am[(size_t)a * 256 + i] = m_run[h];
-          p.aa[(size_t)a * 256 + i] = a_run[h];
-          p.az[(size_t)a * 256 + i] = z_run[h];
-          if (ovf[h]) p.overflow[i] = 1;
-        }
+      if (active && i < p.C) {
+        p.am[(size_t)i * p.n_a + a] = m_run;
+        p.aa[(size_t)i * p.n_a + a] = a_run;
+        p.az[(size_t)i * p.n_a + a] = z_run;
+        if (ovf) p.overflow[i] = 1;
       }
     }
   } else {
     // ===================================================== consumer role: GEMM2 (S += P . E)
     const int c = blockIdx.x - p.n_a;
     const int tau = c % p.n_dt;
-    const int h = (c / p.n_dt) % p.n_rh;
-    const int kap = c / (p.n_dt * p.n_rh);
+    const int kap = c / p.n_dt;
     const int d0 = tau * kDT;
     const int nd = p.d - d0 < kDT ? p.d - d0 : kDT;
     const int nbox = nd / 64;
@@ -411,24 +441,26 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t issued_par[kStages];
         bool issued[kStages];
         for (int s = 0; s < kStages; ++s) issued[s] = false, issued_par[s] = 0;
-        const uint32_t tx = kTileBytes + (uint32_t)nbox * 8192u;
+        const uint32_t pbytes = (uint32_t)p.n_rh * kTileBytes;
+        const uint32_t tx = pbytes + (uint32_t)nbox * 8192u;
         bool ok = true;
         for (int j = 0; j < n_my && ok; ++j) {
           const int t = kap + j * p.ksplit;
           if (!wait_flag(p.ready + t, 1, p)) break;
           fence_proxy_async_global();
-          for (int ks = 0; ks < 2; ++ks) {
+          for (int ks = 0; ks < kVT / 64; ++ks) {
             if (!wait_bar(smem_addr(&bar_empty[stage]), ph ^ 1, p)) { ok = false; break; }
             const uint32_t fb = smem_addr(&bar_full[stage]);
             const uint32_t sb = s_base + stage * kStageBytes;
             mbar_expect_tx(fb, tx);
-            bulk_load(sb, p.pbuf + ((size_t)(t * p.n_rh + h) * 2 + ks) * kTileBytes, kTileBytes, fb);
+            bulk_load(sb, p.pbuf + (size_t)((t * 4 + ks) * p.n_rh) * kTileBytes, pbytes, fb);
             for (int bx = 0; bx < nbox; ++bx)
-              tma_load_2d(sb + kTileBytes + bx * 8192, &tm_emn, d0 + bx * 64, t * kVT + ks * 64, fb);
+              tma_load_2d(sb + 2 * kTileBytes + bx * 8192, &tm_emn, d0 + bx * 64, t * kVT + ks * 64, fb);
             issued[stage] = true;
             issued_par[stage] = ph;
             if (++stage == kStages) { stage = 0; ph ^= 1; }
           }
+          if (ok) atomicAdd(p.consumed + t, 1);
         }
         for (int s = 0; s < kStages; ++s)
           if (issued[s]) wait_bar(smem_addr(&bar_full[s]), issued_par[s], p);
@@ -439,43 +471,47 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t idesc = idesc_bf16_f32(128, nd, 0, 1);
         int stage = 0;
         uint32_t ph = 0;
-        bool ok = true, first = true;
+        bool ok = true;
         for (int j = 0; j < n_my && ok; ++j) {
-          for (int ks = 0; ks < 2; ++ks) {
+          for (int ks = 0; ks < kVT / 64; ++ks) {
             if (!wait_bar(smem_addr(&bar_full[stage]), ph, p)) { ok = false; break; }
             tc_fence_after();
             const uint32_t sb = s_base + stage * kStageBytes;
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
-              const uint64_t adesc = sdesc_sw128(sb + k * 32, 0, 1024);
-              const uint64_t bdesc = sdesc_sw128(sb + kTileBytes + k * 2048, 8192, 1024);
-              mma_bf16(tmem, adesc, bdesc, idesc, first ? 0u : 1u);
-              first = false;
+              const uint64_t bdesc = sdesc_sw128(sb + 2 * kTileBytes + k * 2048, 8192, 1024);
+              const uint32_t acc = (j | ks | k) != 0 ? 1u : 0u;
+              for (int h = 0; h < p.n_rh; ++h) {
+                const uint64_t adesc = sdesc_sw128(sb + h * kTileBytes + k * 32, 0, 1024);
+                mma_bf16(tmem + h * 256, adesc, bdesc, idesc, acc);
+              }
             }
             mma_commit(smem_addr(&bar_empty[stage]));
             if (++stage == kStages) { stage = 0; ph ^= 1; }
           }
         }
-        mma_commit(smem_addr(&bar_tfull[0]));
-        wait_bar(smem_addr(&bar_tfull[0]), 0, p);
+        mma_commit(smem_addr(&bar_tfull));
+        wait_bar(smem_addr(&bar_tfull), 0, p);
       }
       __syncwarp();
     } else {
+      const int hh = (warp - 2) >> 2;
       const int q = warp & 3;
       const int r = q * 32 + lane;
-      const int i = h * 128 + r;
-      const uint32_t lane_off = (uint32_t)(q * 32) << 16;
+      const int i = hh * 128 + r;
+      const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + hh * 256;
       float* dst = p.cpart + ((size_t)kap * 256 + i) * p.d + d0;
-      bool have = n_my > 0;
-      if (have) {
-        have = wait_bar(smem_addr(&bar_tfull[0]), 0, p);
-        have = __all_sync(0xffffffffu, have);  // tcgen05.ld below is warp-collective
+      bool have = n_my > 0 && hh < p.n_rh;
+      if (n_my > 0) {
+        bool got = wait_bar(smem_addr(&bar_tfull), 0, p);
+        got = __all_sync(0xffffffffu, got);  // tcgen05.ld below is warp-collective
+        have = have && got;
         tc_fence_after();
       }
       for (int cc = 0; cc < nd / 32; ++cc) {
         float v[32];
         if (have) {
-          tmem_ld32(tmem + lane_off + cc * 32, v);
+          tmem_ld32(taddr + cc * 32, v);
         } else {
 #pragma unroll
           for (int e = 0; e < 32; ++e) v[e] = 0.f;
@@ -496,23 +532,29 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-// Merge producer statistics and consumer partials for one canvas row (and one
-// 256-column slice of S). A row flagged by the producers is recomputed here
-// from scratch with its true maximum as the reference (fp32, CUDA cores).
+// Merge producer statistics and consumer partials for one canvas row and one
+// slice of kCombineCols columns of S. Row statistics are contiguous per row
+// ([row][producer]); S partials are read once, coalesced. A row flagged by the
+// producers is recomputed here from scratch with its true maximum as the
+// reference (fp32, CUDA cores; slow, only for rows whose logits exceed the
+// sampled reference by more than the safe margin).
+constexpr int kCombineCols = 1024;
+
 __global__ void __launch_bounds__(256) vocab_combine(const Params p, const __nv_bfloat16* __restrict__ h,
                                                      const __nv_bfloat16* __restrict__ emb, int32_t* argmax,
                                                      float* conf, float* lse, __nv_bfloat16* selfcond) {
-  extern __shared__ float hrow[];  // [d] (fixup only)
+  extern __shared__ float hrow[];  // [d] (recompute path only)
   __shared__ float s_m[8], s_z[8], s_r[8], s_pv[256];
   __shared__ int s_a[8];
   const int i = blockIdx.x, slice = blockIdx.y, t = threadIdx.x, lane = t & 31, w = t >> 5;
   float m = -INFINITY, z = 0.f, R = -INFINITY;
   int ai = 0x7fffffff;
+  const size_t rb = (size_t)i * p.n_a;
   for (int a = t; a < p.n_a; a += 256) {
-    const float ma = p.am[(size_t)a * 256 + i];
-    const int aa = p.aa[(size_t)a * 256 + i];
-    z += p.az[(size_t)a * 256 + i];
-    R = fmaxf(R, p.smax[(size_t)a * 256 + i]);
+    const float ma = p.am[rb + a];
+    const int aa = p.aa[rb + a];
+    z += p.az[rb + a];
+    R = fmaxf(R, p.smax[rb + a]);
     if (ma > m || (ma == m && aa < ai)) { m = ma; ai = aa; }
   }
   for (int o = 16; o; o >>= 1) {
@@ -531,22 +573,34 @@ __global__ void __launch_bounds__(256) vocab_combine(const Params p, const __nv_
     R = fmaxf(R, s_r[k]);
   }
   __syncthreads();
-  const int j = slice * 256 + t;
+  const int c0 = slice * kCombineCols;
+  const int c1 = min(p.d, c0 + kCombineCols);
   const bool ovf = p.overflow[i] != 0;
   float out_conf, out_lse;
   if (!ovf) {
     out_conf = expf(m - R) / z;
     out_lse = R + logf(z);
-    if (selfcond && j < p.d) {
-      float acc = 0.f;
-      for (int k = 0; k < p.ksplit; ++k) acc += p.cpart[((size_t)k * 256 + i) * p.d + j];
-      selfcond[(size_t)i * p.d + j] = __float2bfloat16_rn(acc / z);
+    if (selfcond) {
+      const float inv = 1.f / z;
+      for (int j = c0 + 2 * t; j < c1; j += 512) {
+        float2 acc = make_float2(0.f, 0.f);
+        for (int k = 0; k < p.ksplit; ++k) {
+          const float2 v = *reinterpret_cast<const float2*>(p.cpart + ((size_t)k * 256 + i) * p.d + j);
+          acc.x += v.x;
+          acc.y += v.y;
+        }
+        *reinterpret_cast<__nv_bfloat162*>(selfcond + (size_t)i * p.d + j) =
+            __floats2bfloat162_rn(acc.x * inv, acc.y * inv);
+      }
     }
   } else {
     // exact recompute with R = m (the row's true maximum)
     for (int k = t; k < p.d; k += 256) hrow[k] = __bfloat162float(h[(size_t)i * p.d + k]);
     __syncthreads();
-    float zp = 0.f, acc = 0.f;
+    constexpr int kPer = kCombineCols / 256;
+    float zp = 0.f, acc[kPer];
+#pragma unroll
+    for (int q = 0; q < kPer; ++q) acc[q] = 0.f;
     for (int v0 = 0; v0 < p.V; v0 += 256) {
       for (int vv = w * 32; vv < w * 32 + 32; ++vv) {
         const int v = v0 + vv;
@@ -558,9 +612,13 @@ __global__ void __launch_bounds__(256) vocab_combine(const Params p, const __nv_
       }
       __syncthreads();
       zp += s_pv[t];
-      if (j < p.d) {
-        const int nv = p.V - v0 < 256 ? p.V - v0 : 256;
-        for (int vv = 0; vv < nv; ++vv) acc = fmaf(s_pv[vv], __bfloat162float(emb[(size_t)(v0 + vv) * p.d + j]), acc);
+      const int nv = p.V - v0 < 256 ? p.V - v0 : 256;
+#pragma unroll
+      for (int q = 0; q < kPer; ++q) {
+        const int j = c0 + q * 256 + t;
+        if (j < c1)
+          for (int vv = 0; vv < nv; ++vv)
+            acc[q] = fmaf(s_pv[vv], __bfloat162float(emb[(size_t)(v0 + vv) * p.d + j]), acc[q]);
       }
       __syncthreads();
     }
@@ -571,7 +629,13 @@ __global__ void __launch_bounds__(256) vocab_combine(const Params p, const __nv_
     for (int k = 0; k < 8; ++k) zp += s_z[k];
     out_conf = 1.f / zp;
     out_lse = m + logf(zp);
-    if (selfcond && j < p.d) selfcond[(size_t)i * p.d + j] = __float2bfloat16_rn(acc / zp);
+    if (selfcond) {
+#pragma unroll
+      for (int q = 0; q < kPer; ++q) {
+        const int j = c0 + q * 256 + t;
+        if (j < c1) selfcond[(size_t)i * p.d + j] = __float2bfloat16_rn(acc[q] / zp);
+      }
+    }
   }
   if (slice == 0 && t == 0) {
     argmax[i] = ai;
@@ -580,31 +644,12 @@ __global__ void __launch_bounds__(256) vocab_combine(const Params p, const __nv_
   }
 }
 
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-  static std::once_flag once;
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  std::call_once(once, [] {
-    void* f = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = (PFN_cuTensorMapEncodeTiled_v12000)f;
-  });
-  return fn;
-}
-
 // 2D bf16 map over a row-major [rows][cols] matrix, box [box_rows][64], 128-byte swizzle.
 bool make_map(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows, uint32_t box_rows) {
-  auto fn = encode_fn();
-  if (!fn) return false;
-  cuuint64_t dims[2] = {cols, rows};
-  cuuint64_t strides[1] = {cols * 2};
-  cuuint32_t box[2] = {64, box_rows};
-  cuuint32_t estr[2] = {1, 1};
-  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
-                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS;
+  const uint64_t dims[2] = {cols, rows};
+  const uint64_t strides[1] = {cols * 2};
+  const uint32_t box[2] = {64, box_rows};
+  return tmap_bf16_sw128(m, base, 2, dims, strides, box);
 }
 
 }  // namespace
@@ -622,17 +667,19 @@ int vocab_tc_launch(const __nv_bfloat16* h, const __nv_bfloat16* emb, int C, int
   int* st = status_ptr();
   if (!st) return DG_ERR_CUDA;
   CUtensorMap tm_h, tm_ek, tm_emn;
-  if (!make_map(&tm_h, h, d, C, 128) || !make_map(&tm_ek, emb, d, V, 128) || !make_map(&tm_emn, emb, d, V, 64))
+  if (!make_map(&tm_h, h, d, C, 128) || !make_map(&tm_ek, emb, d, V, kVT) || !make_map(&tm_emn, emb, d, V, 64))
     return DG_ERR_CUDA;
   uint8_t* w = (uint8_t*)ws;
   Params p;
   p.C = C; p.V = V; p.d = d;
   p.n_rh = pl.n_rh; p.n_dt = pl.n_dt; p.n_vt = pl.n_vt; p.ksplit = pl.ksplit; p.n_a = pl.n_a;
+  p.window = pl.window;
   int* flags = (int*)(w + L.flags);
   p.ready = flags;
-  p.ref_count = flags + pl.n_vt;
-  p.abort_flag = flags + pl.n_vt + 1;
-  p.overflow = flags + pl.n_vt + 2;
+  p.consumed = flags + pl.n_vt;
+  p.ref_count = flags + 2 * pl.n_vt;
+  p.abort_flag = flags + 2 * pl.n_vt + 1;
+  p.overflow = flags + 2 * pl.n_vt + 2;
   p.smax = (float*)(w + L.smax);
   p.am = (float*)(w + L.am);
   p.aa = (int*)(w + L.aa);
@@ -662,7 +709,7 @@ int vocab_tc_launch(const __nv_bfloat16* h, const __nv_bfloat16* emb, int C, int
   cfg.numAttrs = 1;
   DG_CUDA_TRY(cudaLaunchKernelEx(&cfg, vocab_main, tm_h, tm_ek, tm_emn, p));
 
-  dim3 cgrid(C, pl.n_dt);
+  dim3 cgrid(C, (d + kCombineCols - 1) / kCombineCols);
   const size_t csmem = (size_t)d * sizeof(float);
   vocab_combine<<<cgrid, 256, csmem, s>>>(p, h, emb, argmax, conf, lse, selfcond);
   DG_LAUNCH_CHECK();

@@ -107,6 +107,26 @@ def test_canvas_attn_bf16(lib, mask, C, Hq, Hkv, hd, P):
     _status_ok()
 
 
+@pytest.mark.parametrize("mask", [B.DG_MASK_BIDIR, B.DG_MASK_CAUSAL_BLOCK])
+def test_canvas_attn_late_dominant_key(lib, mask):
+    """A key in a late tile scores far above everything in the first tile, so
+    the running reference must move and O be rescaled."""
+    C, Hq, Hkv, hd, P = 96, 4, 2, 128, 1000
+    g = torch.Generator().manual_seed(5)
+    q0 = torch.randn(hd, generator=g)
+    q = (q0 + 0.5 * torch.randn(C, Hq, hd, generator=g)).to(torch.bfloat16)
+    k = torch.randn(Hkv, P + C, hd, generator=g)
+    v = torch.randn(Hkv, P + C, hd, generator=g)
+    k[:, 900] = 4.0 * q0
+    k, v = k.to(torch.bfloat16), v.to(torch.bfloat16)
+    kn, vn = k[:, P:].contiguous(), v[:, P:].contiguous()
+    out, lse = B.canvas_attn(q.cuda(), k.cuda(), v.cuda(), P, kn.cuda(), vn.cuda(), mask=mask)
+    ro, rl = oracle.canvas_attention(_np(q), _np(k), _np(v), P, _np(kn), _np(vn), causal=mask == 1)
+    assert_rows_close(_np(out).reshape(C * Hq, hd), ro.reshape(C * Hq, hd), what="attn out")
+    assert np.abs(_np(lse) - rl).max() <= LSE_ABS
+    _status_ok()
+
+
 def test_canvas_attn_f32_tiny(lib):
     w = WORKLOADS["tiny_f32"]
     k, v = synth.kv_prefix(w.Hkv, w.cap, w.hd, w.prefix, w.seed, dtype=torch.float32)
