@@ -31,6 +31,9 @@ _SIGS = {
     "dg_canvas_attn_workspace_size": (_c_sz, [_c_int, _c_int, _c_int, _c_int, _c_i64, _c_int]),
     "dg_canvas_attn": (_c_int, [_p, _p, _p, _c_i64, _c_i64, _p, _p, _p, _p, _c_int, _c_int, _c_int, _c_int, _c_f,
                                 _c_int, _c_int, _p, _c_sz, _p]),
+    "dg_canvas_attn_noalloc": (_c_int, [_p, _p, _p, _c_i64, _c_i64, _p, _p, _p, _p, _c_int, _c_int, _c_int, _c_int,
+                                        _c_f, _c_int, _c_int, _p]),
+    "dg_canvas_attn_noalloc_max_scratch": (_c_sz, []),
     "dg_vocab_step_workspace_size": (_c_sz, [_c_int, _c_int, _c_int, _c_int]),
     "dg_vocab_step": (_c_int, [_p, _p, _c_int, _c_int, _c_int, _c_int, _p, _p, _p, _p, _p, _c_sz, _p]),
     "dg_renoise": (_c_int, [_p, _p, _p, _c_int, _c_int, _c_f, _c_u64, _c_u32, _c_i64, _p, _p]),
@@ -135,6 +138,25 @@ def canvas_attn(q, k_cache, v_cache, prefix_len, k_canvas, v_canvas, out=None, l
                                _ptr(v_canvas), _ptr(out), _ptr(lse), C, Hq, Hkv, hd, float(scale), dt, mask,
                                _ptr(workspace), ws_bytes, _stream(stream))
     _check("dg_canvas_attn", rc)
+    return out, lse
+
+
+def canvas_attn_noalloc(q, k_cache, v_cache, prefix_len, k_canvas, v_canvas, out=None, lse=None, scale=-1.0,
+                        mask=DG_MASK_BIDIR, stream=None):
+    """dg_canvas_attn without a workspace: for callers that cannot allocate
+    device memory (the scratch is a fixed array inside the library)."""
+    for t, n in ((q, "q"), (k_cache, "k_cache"), (v_cache, "v_cache"), (k_canvas, "k_canvas"), (v_canvas, "v_canvas")):
+        _need(t, n)
+    C, Hq, hd = q.shape
+    Hkv, cap = k_cache.shape[0], k_cache.shape[1]
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((Hq, C), dtype=torch.float32, device=q.device)
+    rc = load().dg_canvas_attn_noalloc(_ptr(q), _ptr(k_cache), _ptr(v_cache), cap, prefix_len, _ptr(k_canvas),
+                                       _ptr(v_canvas), _ptr(out), _ptr(lse), C, Hq, Hkv, hd, float(scale),
+                                       _dtype_code(q), mask, _stream(stream))
+    _check("dg_canvas_attn_noalloc", rc)
     return out, lse
 
 

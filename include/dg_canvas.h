@@ -99,6 +99,24 @@ DG_API int dg_canvas_attn(const void* q, const void* k_cache, const void* v_cach
                    int C, int Hq, int Hkv, int hd, float scale, int dtype, int mask,
                    void* workspace, size_t workspace_bytes, void* stream);
 
+/* Canvas attention for callers that cannot allocate device memory (code
+ * running during stream capture, hosts that own every device allocation,
+ * plugins given no scratch buffer). The explainer pages have no counterpart:
+ * this is a deployment variant of dg_canvas_attn, same arguments and results
+ * minus the workspace. Its split-KV scratch is a fixed array inside the
+ * library's device image (dg_canvas_attn_noalloc_max_scratch() bytes, 16 MiB),
+ * reserved on every GPU that loads the library until the process exits.
+ *   - Returns DG_ERR_WORKSPACE if the shape needs more scratch than that.
+ *   - The first call on a device looks up the array's device address with the
+ *     device current; make that first call before any stream capture.
+ *   - All calls share the array: calls that may overlap on the GPU race on it.
+ *   - Allocates nothing (no cudaMalloc, no library allocator). */
+DG_API int dg_canvas_attn_noalloc(const void* q, const void* k_cache, const void* v_cache, int64_t cap,
+                                  int64_t prefix_len, const void* k_canvas, const void* v_canvas, void* out,
+                                  float* lse, int C, int Hq, int Hkv, int hd, float scale, int dtype, int mask,
+                                  void* stream);
+DG_API size_t dg_canvas_attn_noalloc_max_scratch(void);
+
 /* ---------------------------------------------------------------- vocabulary step
  * For each canvas position i (row of h):
  *   logits l_i = h_i . emb^T            (emb is the tied token-embedding table)
