@@ -6,21 +6,24 @@
 // denoising": in denoising mode every canvas query sees every canvas token
 // and the KV cache; in prefill mode attention is causal.
 //
-// One CTA per (128 query rows, KV head, key split). The Hq/Hkv query heads of
-// one KV head are stacked (row = position * group + head-in-group), so a K/V
-// tile feeds all of them. Keys come in tiles of 128: first the cache rows
-// [0, P), then the canvas rows [0, C); tiles never straddle the two, and the
-// tensor maps' row extents are exactly P and C, so rows past the end read as
-// zeros. Per tile:
-//   S = Q K^T      tcgen05, into one of two TMEM buffers (128 columns each)
-//   softmax        4 warps, one query row per thread: row max, a per-row
-//                  reference kept fixed unless a tile's max exceeds it by
-//                  2^8 (then O and the row sum are rescaled through TMEM),
-//                  P = exp2(s - ref) in bf16 written to shared memory in the
-//                  128-byte-swizzled K-major operand layout
-//   O += P V       tcgen05, V read MN-major, O accumulated in TMEM.
-// S(j+1) is issued before PV(j), so the tensor core works while the softmax
-// warps do. Splits write fp32 partials (O, lse) merged by attn_combine.
+// One CTA per (256 query rows = two query tiles, KV head, key split). The
+// Hq/Hkv query heads of one KV head are stacked (row = position * group +
+// head-in-group), so a K/V tile feeds all of them. Keys come in tiles of 128:
+// first the cache rows [0, P), then the canvas rows [0, C); tiles never
+// straddle the two, and the tensor maps' row extents are exactly P and C, so
+// rows past the end read as zeros. K and V tiles stream through a 3-slot TMA
+// ring. For each key tile and each query tile q:
+//   S_q = Q_q K^T   tcgen05 into TMEM (128 columns per query tile)
+//   softmax         4 warps per query tile, one row per thread: one 128-column
+//                   TMEM load (after which S_q may be overwritten), row max, a
+//                   per-row reference kept unless a tile's max exceeds it by
+//                   2^8 (then O_q and the row sum are rescaled through TMEM),
+//                   P = exp2(s - ref) in bf16 into shared memory in the
+//                   128-byte-swizzled K-major operand layout
+//   O_q += P_q V    tcgen05, V read MN-major, O_q accumulated in TMEM.
+// The MMA warp interleaves the two query tiles (S0(j+1) PV0(j) S1(j+1)
+// PV1(j)), so one softmax group works while the tensor core serves the other.
+// Splits write fp32 partials (O, lse) merged by attn_combine.
 // Every wait is bounded (about two seconds); on expiry the CTA latches
 // DG_ERR_TIMEOUT, drains what it issued, frees TMEM and returns.
 #include <cudaTypedefs.h>
@@ -39,13 +42,14 @@ namespace {
 using namespace sm100;
 
 constexpr int kHD = 128;
-constexpr int kBM = 128;
+constexpr int kBM = 256;  // two query tiles of 128 rows
 constexpr int kBN = 128;
-constexpr int kThreads = 192;  // warp 0: TMA, warp 1: MMA, warps 2..5: softmax + epilogue
+constexpr int kThreads = 320;  // warp 0: TMA, warp 1: MMA, warps 2..5 / 6..9: softmax of query tile 0 / 1
+constexpr int kRing = 3;       // K/V tile slots (K0 V0 K1 V1 ... in order)
 constexpr uint32_t kChunk = 16384;  // [128 rows x 64 bf16] swizzled block
 constexpr uint32_t kTile = 2 * kChunk;
-// shared memory: Q | K[2] | V[2] | P[2]
-constexpr uint32_t kOffQ = 0, kOffK = kTile, kOffV = 3 * kTile, kOffP = 5 * kTile, kSmem = 7 * kTile;
+// shared memory: Q[2] | ring[3] | P[2]
+constexpr uint32_t kOffQ = 0, kOffRing = 2 * kTile, kOffP = 5 * kTile, kSmem = 7 * kTile;
 constexpr float kRescale = 8.f;  // log2 units
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr long long kTimeoutCycles = 4000000000ll;
@@ -85,13 +89,15 @@ __device__ bool wait_bar(uint32_t bar, uint32_t parity, const Ctl& c) {
   }
 }
 
-__device__ __forceinline__ bool sm_any(bool v) {
+// Barrier over the 128 threads of softmax group q (named barrier 1 + q) that
+// ORs a predicate, so the group takes the same branch after a bounded wait.
+__device__ __forceinline__ bool grp_any(int q, bool v) {
   uint32_t r;
   asm volatile(
-      "{\n .reg .pred pi, po;\n setp.ne.u32 pi, %1, 0;\n barrier.red.or.pred po, 1, 128, pi;\n"
+      "{\n .reg .pred pi, po;\n setp.ne.u32 pi, %1, 0;\n barrier.red.or.pred po, %2, 128, pi;\n"
       " selp.u32 %0, 1, 0, po;\n}\n"
       : "=r"(r)
-      : "r"((uint32_t)v)
+      : "r"((uint32_t)v), "r"(1 + q)
       : "memory");
   return r != 0;
 }
@@ -107,8 +113,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_tc(const __grid_constant__ CUtensorMap tk_c, const __grid_constant__ CUtensorMap tv_c,
                 const __grid_constant__ CUtensorMap tk_n, const __grid_constant__ CUtensorMap tv_n, const TcArgs a) {
   extern __shared__ __align__(1024) uint8_t smem_dyn[];
-  __shared__ __align__(8) uint64_t k_full[2], k_empty[2], v_full[2], v_empty[2], s_full[2], s_empty[2], p_full[2],
-      p_empty[2], o_done, drain;
+  __shared__ __align__(8) uint64_t ring_full[kRing], ring_empty[kRing], s_full[2], s_free[2], p_full[2], p_free[2],
+      drain;
   __shared__ uint32_t tmem_slot;
   __shared__ int abort_flag;
 
@@ -132,17 +138,16 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (tid == 0) {
     abort_flag = 0;
-    for (int s = 0; s < 2; ++s) {
-      mbar_init(smem_addr(&k_full[s]), 1);
-      mbar_init(smem_addr(&k_empty[s]), 1);
-      mbar_init(smem_addr(&v_full[s]), 1);
-      mbar_init(smem_addr(&v_empty[s]), 1);
-      mbar_init(smem_addr(&s_full[s]), 1);
-      mbar_init(smem_addr(&s_empty[s]), 128);
-      mbar_init(smem_addr(&p_full[s]), 128);
-      mbar_init(smem_addr(&p_empty[s]), 1);
+    for (int s = 0; s < kRing; ++s) {
+      mbar_init(smem_addr(&ring_full[s]), 1);
+      mbar_init(smem_addr(&ring_empty[s]), 1);
     }
-    mbar_init(smem_addr(&o_done), 1);
+    for (int q = 0; q < 2; ++q) {
+      mbar_init(smem_addr(&s_full[q]), 1);
+      mbar_init(smem_addr(&s_free[q]), 128);
+      mbar_init(smem_addr(&p_full[q]), 128);
+      mbar_init(smem_addr(&p_free[q]), 1);
+    }
     mbar_init(smem_addr(&drain), 1);
     fence_mbar_init();
     if (a.P > 0) {
@@ -156,14 +161,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_alloc(smem_addr(&tmem_slot), 512);
     tmem_relinquish();
   }
-  // Q tile -> shared memory in the swizzled K-major layout (all threads)
+  // both Q tiles -> shared memory in the swizzled K-major layout (all threads)
   for (int idx = tid; idx < kBM * 16; idx += kThreads) {
     const int r = idx >> 4, ch = idx & 15;
     const int64_t R = (int64_t)mblk * kBM + r;
     const bool ok = R < M;
     const int64_t i = ok ? R / a.grp : 0, j = ok ? R % a.grp : 0;
     const __nv_bfloat16* src = a.q + ((i * a.Hq + (int64_t)g * a.grp + j) * kHD + ch * 8);
-    const uint32_t dst = sbase + kOffQ + (ch >> 3) * kChunk + r * 128 + ((((uint32_t)ch & 7u) ^ ((uint32_t)r & 7u)) << 4);
+    const int qt = r >> 7, rr = r & 127;
+    const uint32_t dst = sbase + kOffQ + qt * kTile + (ch >> 3) * kChunk + rr * 128 +
+                         ((((uint32_t)ch & 7u) ^ ((uint32_t)rr & 7u)) << 4);
     const int sz = ok ? 16 : 0;
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(dst), "l"(src), "r"(sz) : "memory");
   }
@@ -173,90 +180,88 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = tmem_slot;
-  const uint32_t tS = tmem, tO = tmem + 256;
 
   if (warp == 0) {
-    // ------------------------------------------------ TMA producer
+    // ------------------------------------------------ TMA producer: K0 V0 K1 V1 ... through a 3-slot ring
     if (lane == 0 && n > 0) {
-      bool issued_k[2] = {false, false}, issued_v[2] = {false, false};
-      uint32_t par_k[2] = {0, 0}, par_v[2] = {0, 0};
-      for (int jj = 0; jj < n; ++jj) {
-        const int t = T0 + jj, slot = jj & 1;
-        const uint32_t ph = (uint32_t)(jj >> 1) & 1u;
+      bool issued[kRing] = {false, false, false};
+      uint32_t par[kRing] = {0, 0, 0};
+      for (int it = 0; it < 2 * n; ++it) {
+        const int jj = it >> 1, t = T0 + jj;
+        const bool is_v = it & 1;
+        const int slot = it % kRing;
+        const uint32_t ph = (uint32_t)(it / kRing) & 1u;
         const bool cache = t < a.n_cache_tiles;
         const int y = cache ? t * kBN : (t - a.n_cache_tiles) * kBN;
-        const CUtensorMap* mk = cache ? &tk_c : &tk_n;
-        const CUtensorMap* mv = cache ? &tv_c : &tv_n;
-        if (!wait_bar(smem_addr(&k_empty[slot]), ph ^ 1u, ctl)) break;
-        mbar_expect_tx(smem_addr(&k_full[slot]), kTile);
-        tma_load_3d(sbase + kOffK + slot * kTile, mk, 0, y, g, smem_addr(&k_full[slot]));
-        tma_load_3d(sbase + kOffK + slot * kTile + kChunk, mk, 64, y, g, smem_addr(&k_full[slot]));
-        issued_k[slot] = true;
-        par_k[slot] = ph;
-        if (!wait_bar(smem_addr(&v_empty[slot]), ph ^ 1u, ctl)) break;
-        mbar_expect_tx(smem_addr(&v_full[slot]), kTile);
-        tma_load_3d(sbase + kOffV + slot * kTile, mv, 0, y, g, smem_addr(&v_full[slot]));
-        tma_load_3d(sbase + kOffV + slot * kTile + kChunk, mv, 64, y, g, smem_addr(&v_full[slot]));
-        issued_v[slot] = true;
-        par_v[slot] = ph;
+        const CUtensorMap* mp = cache ? (is_v ? &tv_c : &tk_c) : (is_v ? &tv_n : &tk_n);
+        if (!wait_bar(smem_addr(&ring_empty[slot]), ph ^ 1u, ctl)) break;
+        mbar_expect_tx(smem_addr(&ring_full[slot]), kTile);
+        tma_load_3d(sbase + kOffRing + slot * kTile, mp, 0, y, g, smem_addr(&ring_full[slot]));
+        tma_load_3d(sbase + kOffRing + slot * kTile + kChunk, mp, 64, y, g, smem_addr(&ring_full[slot]));
+        issued[slot] = true;
+        par[slot] = ph;
       }
-      for (int s = 0; s < 2; ++s) {
-        if (issued_k[s]) wait_bar(smem_addr(&k_full[s]), par_k[s], ctl);
-        if (issued_v[s]) wait_bar(smem_addr(&v_full[s]), par_v[s], ctl);
-      }
+      for (int s = 0; s < kRing; ++s)
+        if (issued[s]) wait_bar(smem_addr(&ring_full[s]), par[s], ctl);
     }
     __syncwarp();
   } else if (warp == 1) {
     // ------------------------------------------------ MMA issuer
+    // order: S0(0) S1(0) | S0(1) PV0(0) S1(1) PV1(0) | S0(2) PV0(1) S1(2) PV1(1) | ...
     if (lane == 0 && n > 0) {
       const uint32_t id_s = idesc_bf16_f32(128, kBN, 0, 0);
       const uint32_t id_o = idesc_bf16_f32(128, kHD, 0, 1);
-      auto issue_s = [&](int jj) -> bool {
-        const int slot = jj & 1;
-        const uint32_t ph = (uint32_t)(jj >> 1) & 1u;
-        if (!wait_bar(smem_addr(&k_full[slot]), ph, ctl)) return false;
-        if (!wait_bar(smem_addr(&s_empty[slot]), ph ^ 1u, ctl)) return false;
+      auto issue_s = [&](int q, int jj) -> bool {
+        const int it = 2 * jj, slot = it % kRing;
+        if (!wait_bar(smem_addr(&ring_full[slot]), (uint32_t)(it / kRing) & 1u, ctl)) return false;
+        if (jj > 0 && !wait_bar(smem_addr(&s_free[q]), (uint32_t)(jj - 1) & 1u, ctl)) return false;
         tc_fence_after();
-        const uint32_t kb = sbase + kOffK + slot * kTile;
+        const uint32_t kb = sbase + kOffRing + slot * kTile, qb = sbase + kOffQ + q * kTile;
 #pragma unroll
         for (int kk = 0; kk < kHD / 16; ++kk) {
-          const uint64_t ad = sdesc_sw128(sbase + kOffQ + (kk >> 2) * kChunk + (kk & 3) * 32, 0, 1024);
+          const uint64_t ad = sdesc_sw128(qb + (kk >> 2) * kChunk + (kk & 3) * 32, 0, 1024);
           const uint64_t bd = sdesc_sw128(kb + (kk >> 2) * kChunk + (kk & 3) * 32, 0, 1024);
-          mma_bf16(tS + slot * 128, ad, bd, id_s, kk > 0);
+          mma_bf16(tmem + q * 128, ad, bd, id_s, kk > 0);
         }
-        mma_commit(smem_addr(&k_empty[slot]));
-        mma_commit(smem_addr(&s_full[slot]));
+        mma_commit(smem_addr(&s_full[q]));
+        if (q == 1) mma_commit(smem_addr(&ring_empty[slot]));  // K(jj) consumed by both tiles
         return true;
       };
-      bool ok = issue_s(0);
-      for (int jj = 0; jj < n && ok; ++jj) {
-        if (jj + 1 < n && !issue_s(jj + 1)) break;
-        const int slot = jj & 1;
-        const uint32_t ph = (uint32_t)(jj >> 1) & 1u;
-        if (!wait_bar(smem_addr(&p_full[slot]), ph, ctl)) break;
-        if (!wait_bar(smem_addr(&v_full[slot]), ph, ctl)) break;
+      auto issue_pv = [&](int q, int jj) -> bool {
+        const int it = 2 * jj + 1, slot = it % kRing;
+        if (!wait_bar(smem_addr(&ring_full[slot]), (uint32_t)(it / kRing) & 1u, ctl)) return false;
+        if (!wait_bar(smem_addr(&p_full[q]), (uint32_t)jj & 1u, ctl)) return false;
         tc_fence_after();
-        const uint32_t pb = sbase + kOffP + slot * kTile, vb = sbase + kOffV + slot * kTile;
+        const uint32_t pb = sbase + kOffP + q * kTile, vb = sbase + kOffRing + slot * kTile;
 #pragma unroll
         for (int kk = 0; kk < kBN / 16; ++kk) {
           const uint64_t ad = sdesc_sw128(pb + (kk >> 2) * kChunk + (kk & 3) * 32, 0, 1024);
           const uint64_t bd = sdesc_sw128(vb + kk * 2048, kChunk, 1024);
-          mma_bf16(tO, ad, bd, id_o, (jj > 0 || kk > 0) ? 1u : 0u);
+          mma_bf16(tmem + 256 + q * 128, ad, bd, id_o, (jj > 0 || kk > 0) ? 1u : 0u);
         }
-        mma_commit(smem_addr(&v_empty[slot]));
-        mma_commit(smem_addr(&p_empty[slot]));
-        mma_commit(smem_addr(&o_done));
+        mma_commit(smem_addr(&p_free[q]));
+        if (q == 1) mma_commit(smem_addr(&ring_empty[slot]));  // V(jj) consumed by both tiles
+        return true;
+      };
+      bool ok = issue_s(0, 0) && issue_s(1, 0);
+      for (int jj = 0; jj < n && ok; ++jj) {
+        if (jj + 1 < n && !issue_s(0, jj + 1)) break;
+        if (!issue_pv(0, jj)) break;
+        if (jj + 1 < n && !issue_s(1, jj + 1)) break;
+        if (!issue_pv(1, jj)) break;
       }
       mma_commit(smem_addr(&drain));
       wait_bar(smem_addr(&drain), 0, ctl);
     }
     __syncwarp();
   } else {
-    // ------------------------------------------------ softmax + epilogue (one query row per thread)
+    // ------------------------------------------------ softmax + epilogue: group q owns query tile q
+    const int q = (warp - 2) >> 2;
     const int q4 = warp & 3;
     const int r = q4 * 32 + lane;
     const uint32_t loff = (uint32_t)(q4 * 32) << 16;
-    const int64_t R = (int64_t)mblk * kBM + r;
+    const uint32_t tS = tmem + q * 128, tO = tmem + 256 + q * 128;
+    const int64_t R = (int64_t)mblk * kBM + q * 128 + r;
     const bool row_ok = R < M;
     const int64_t i = row_ok ? R / a.grp : 0;
     const int64_t h = (int64_t)g * a.grp + (row_ok ? R % a.grp : 0);
@@ -264,9 +269,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     int done_tiles = 0;
     for (int jj = 0; jj < n; ++jj) {
-      const int t = T0 + jj, slot = jj & 1;
-      const uint32_t ph = (uint32_t)(jj >> 1) & 1u;
-      // visible columns of this tile for this row: [0, lim)
+      const int t = T0 + jj;
       int lim;
       if (t < a.n_cache_tiles) {
         lim = (int)min64(kBN, a.P - (int64_t)t * kBN);
@@ -276,14 +279,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (a.causal) lim = (int)min64(lim, i - c0 + 1);
       }
       if (!row_ok || lim < 0) lim = 0;
-      const bool got = wait_bar(smem_addr(&s_full[slot]), ph, ctl);
-      if (sm_any(!got)) { ok = false; break; }
+      const bool got = wait_bar(smem_addr(&s_full[q]), (uint32_t)jj & 1u, ctl);
+      if (grp_any(q, !got)) { ok = false; break; }
       tc_fence_after();
-      const uint32_t sa = tS + loff + slot * 128;
       float v[kBN];
-      tmem_ld128(sa, v);  // the whole S row of this tile, one load, one wait
-      const bool full = lim == kBN;
-      if (!full) {
+      tmem_ld128(tS + loff, v);  // the whole S row of this tile, one load, one wait
+      tc_fence_before();
+      mbar_arrive(smem_addr(&s_free[q]));  // the MMA may overwrite S now
+      if (lim < kBN) {
 #pragma unroll
         for (int e = 0; e < kBN; ++e)
           if (e >= lim) v[e] = -INFINITY;
@@ -308,33 +311,29 @@ __global__ void __launch_bounds__(kThreads, 1)
           l *= factor;
         }
       }
-      if (__any_sync(0xffffffffu, need)) {
-        // O must hold every PV issued so far before it is rescaled in place
-        const bool od = wait_bar(smem_addr(&o_done), (uint32_t)(jj - 1) & 1u, ctl);
-        if (!__all_sync(0xffffffffu, od)) { ok = false; }
+      // PV(jj-1) must be complete both before P is overwritten and before O is rescaled
+      if (jj > 0) {
+        const bool pf = wait_bar(smem_addr(&p_free[q]), (uint32_t)(jj - 1) & 1u, ctl);
+        if (grp_any(q, !pf)) { ok = false; break; }
         tc_fence_after();
-        if (ok) {
+      }
+      if (__any_sync(0xffffffffu, need)) {
 #pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            float o[32];
-            tmem_ld32(tO + loff + c * 32, o);
+        for (int c = 0; c < 4; ++c) {
+          float o[32];
+          tmem_ld32(tO + loff + c * 32, o);
 #pragma unroll
-            for (int e = 0; e < 32; ++e) o[e] *= factor;
-            tmem_st32(tO + loff + c * 32, o);
-          }
+          for (int e = 0; e < 32; ++e) o[e] *= factor;
+          tmem_st32(tO + loff + c * 32, o);
         }
       }
-      if (sm_any(!ok)) { ok = false; break; }
-      const bool pe = wait_bar(smem_addr(&p_empty[slot]), ph ^ 1u, ctl);
-      if (sm_any(!pe)) { ok = false; break; }
-      uint8_t* prow = sm + kOffP + slot * kTile + r * 128;
+      uint8_t* prow = sm + kOffP + q * kTile + r * 128;
       const float rr = ref == -INFINITY ? 0.f : ref;
       float sum8[8];
 #pragma unroll
       for (int e = 0; e < 8; ++e) sum8[e] = 0.f;
 #pragma unroll
       for (int c = 0; c < kBN / 8; ++c) {
-        // 8 keys -> one 16-byte piece of the swizzled P row
         float p8[8];
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
@@ -347,16 +346,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       l += ((sum8[0] + sum8[1]) + (sum8[2] + sum8[3])) + ((sum8[4] + sum8[5]) + (sum8[6] + sum8[7]));
       tc_fence_before();
-      mbar_arrive(smem_addr(&s_empty[slot]));
       fence_proxy_async_smem();
-      mbar_arrive(smem_addr(&p_full[slot]));
+      mbar_arrive(smem_addr(&p_full[q]));
       done_tiles = jj + 1;
     }
     // epilogue
     bool have = ok && done_tiles == n && n > 0;
     if (have) {
-      const bool od = wait_bar(smem_addr(&o_done), (uint32_t)(n - 1) & 1u, ctl);
-      have = !sm_any(!od);
+      const bool od = wait_bar(smem_addr(&p_free[q]), (uint32_t)(n - 1) & 1u, ctl);
+      have = !grp_any(q, !od);
       tc_fence_after();
     }
     const float inv = l > 0.f ? 1.f / l : 0.f;

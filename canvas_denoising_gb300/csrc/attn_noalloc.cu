@@ -8,7 +8,7 @@
 // point keeps its split-KV scratch in a fixed array in device memory that is
 // part of the library image itself.
 //
-// The array is kAttnScratchBytes (16 MiB). Every GPU that loads the library
+// The array is kAttnScratchBytes (32 MiB). Every GPU that loads the library
 // keeps that memory reserved until the process exits. All calls share the one
 // array: calls that can overlap on the GPU (different streams without
 // ordering between them) race on it and must not be issued. Nothing in the
@@ -27,7 +27,7 @@
 namespace dg {
 namespace {
 
-constexpr size_t kAttnScratchBytes = 16u << 20;
+constexpr size_t kAttnScratchBytes = 32u << 20;
 
 static __device__ __align__(256) unsigned char g_attn_scratch[kAttnScratchBytes];
 

@@ -5,7 +5,7 @@
 #include <cuda_bf16.h>
 #include <stdint.h>
 
-#include "../../include/dg_canvas.h"
+#include "dg_canvas.h"
 
 namespace dg {
 

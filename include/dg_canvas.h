@@ -104,7 +104,7 @@ DG_API int dg_canvas_attn(const void* q, const void* k_cache, const void* v_cach
  * plugins given no scratch buffer). The explainer pages have no counterpart:
  * this is a deployment variant of dg_canvas_attn, same arguments and results
  * minus the workspace. Its split-KV scratch is a fixed array inside the
- * library's device image (dg_canvas_attn_noalloc_max_scratch() bytes, 16 MiB),
+ * library's device image (dg_canvas_attn_noalloc_max_scratch() bytes, 32 MiB),
  * reserved on every GPU that loads the library until the process exits.
  *   - Returns DG_ERR_WORKSPACE if the shape needs more scratch than that.
  *   - The first call on a device looks up the array's device address with the

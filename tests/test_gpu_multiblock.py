@@ -1,0 +1,70 @@
+"""Block diffusion through the driver: several canvases, each denoised for a
+few steps and then appended to the cache, checked step by step against the
+oracle (teacher-forced: the oracle sees the same inputs and cache prefix)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from canvas_denoising_gb300 import synth
+from canvas_denoising_gb300.driver import CanvasDenoiser, generate
+from tests.parity import FLAG_BUDGET, LSE_ABS, assert_rows_close, decision_flags
+
+pytestmark = pytest.mark.gpu
+
+
+def _np(t):
+    return t.detach().float().cpu().numpy() if t.dtype == torch.bfloat16 else t.detach().cpu().numpy()
+
+
+@pytest.mark.parametrize("C,V,d,Hq,Hkv,P0,blocks,steps", [(128, 8192, 256, 4, 2, 256, 3, 2),
+                                                          (256, 32768, 1024, 8, 4, 1024, 2, 2)])
+def test_generate_matches_oracle_each_step(lib, C, V, d, Hq, Hkv, P0, blocks, steps):
+    hd, thr, seed, alpha = 128, 0.3, 7, 6.0 if d == 256 else 26.0
+    std = 0.1 if d == 256 else 0.02
+    emb = synth.embedding(V, d, seed, std=std)
+    k, v = synth.kv_prefix(Hkv, P0 + blocks * C, hd, P0, seed)
+    emb_d, k_d, v_d = emb.cuda(), k.cuda(), v.cuda()
+    mirror = {"k": _np(k), "v": _np(v), "blocks": 0}  # host copy of the cache, appended as the GPU appends
+    den = CanvasDenoiser(emb_d, k_d, v_d, P0, C, Hq, thr, seed)
+    inputs = {}
+
+    def backbone(b, s, tokens, selfcond):
+        q, kc, vc = synth.canvas_qkv(C, Hq, Hkv, hd, seed, block=b, step=s)
+        h = synth.hidden(emb, synth.targets(C, V, seed, block=b), alpha, seed, block=b, step=s)
+        inputs[(b, s)] = (q, kc, vc, h)
+        return q.cuda(), kc.cuda(), vc.cuda(), h.cuda()
+
+    stats = {"flagged": 0, "total": 0}
+
+    def sync_mirror(upto):
+        while mirror["blocks"] < upto:
+            b0 = mirror["blocks"]
+            _, kc0, vc0, _ = inputs[(b0, steps)]
+            mirror["k"], mirror["v"], _ = oracle.kv_append(mirror["k"], mirror["v"], P0 + b0 * C, _np(kc0), _np(vc0))
+            mirror["blocks"] += 1
+
+    def on_step(b, s, dn):
+        sync_mirror(b)
+        assert dn.len == P0 + b * C
+        q, kc, vc, h = inputs[(b, s)]
+        o = dn.out
+        ro, rl = oracle.canvas_attention(_np(q), mirror["k"], mirror["v"], dn.len, _np(kc), _np(vc))
+        assert_rows_close(_np(o.attn_out).reshape(-1, hd), ro.reshape(-1, hd), what=f"attn b{b}s{s}")
+        assert np.abs(_np(o.attn_lse) - rl).max() <= LSE_ABS
+        rv = oracle.vocab_step(_np(h), _np(emb))
+        assert_rows_close(_np(o.selfcond), rv["selfcond"], what=f"selfcond b{b}s{s}")
+        tok, _ = oracle.renoise(rv["argmax"], rv["conf"].astype(np.float32), V, thr, seed, s, dn.len)
+        fl = decision_flags(rv, thr)
+        assert ((_np(dn.tokens) == tok) | fl).all(), f"tokens b{b}s{s}"
+        stats["flagged"] += int(fl.sum())
+        stats["total"] += C
+
+    finished = generate(den, blocks, steps, backbone, on_step=on_step)
+    torch.cuda.synchronize()
+    assert len(finished) == blocks and den.len == P0 + blocks * C
+    # the cache holds the prefix and every finished canvas's K/V, in order
+    sync_mirror(blocks)
+    np.testing.assert_array_equal(_np(k_d), mirror["k"])
+    np.testing.assert_array_equal(_np(v_d), mirror["v"])
+    assert stats["flagged"] <= FLAG_BUDGET * stats["total"]
