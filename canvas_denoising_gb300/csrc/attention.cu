@@ -373,31 +373,51 @@ __global__ void attn_fwd_f32(const float* __restrict__ q, const float* __restric
 }  // namespace
 
 // Merge split partials: lse = log sum_s exp(lse_s); O = sum_s exp(lse_s - lse) O_s.
-// One warp per (position, head): the lanes first hold the split weights
-// (splits <= 64, two per lane), then each lane owns HD/32 output columns.
+// One warp per (position, head). Every lane reads all split lse values (the
+// same addresses across the warp: broadcast loads) and forms the weights
+// itself, so the column loop below is a chain of independent loads.
+constexpr int kMaxSplits = 64;
+
 template <typename OutT>
-__global__ void attn_combine(const float* __restrict__ part_o, const float* __restrict__ part_lse, OutT* out,
-                             float* lse, int C, int Hq, int HD, int splits) {
-  int64_t w = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-  int lane = threadIdx.x & 31;
+__global__ void __launch_bounds__(256) attn_combine(const float* __restrict__ part_o,
+                                                    const float* __restrict__ part_lse, OutT* out, float* lse, int C,
+                                                    int Hq, int HD, int splits) {
+  const int64_t w = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
   if (w >= (int64_t)C * Hq) return;
-  int64_t i = w / Hq, h = w % Hq;
-  float l0 = lane < splits ? part_lse[((int64_t)lane * Hq + h) * C + i] : -INFINITY;
-  float l1 = lane + 32 < splits ? part_lse[((int64_t)(lane + 32) * Hq + h) * C + i] : -INFINITY;
-  float mx = fmaxf(l0, l1);
-  for (int o = 16; o; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+  const int64_t i = w / Hq, h = w % Hq;
+  float lw[kMaxSplits];
+  float mx = -INFINITY;
+#pragma unroll 8
+  for (int s = 0; s < splits; ++s) {
+    lw[s] = __ldg(part_lse + ((int64_t)s * Hq + h) * C + i);
+    mx = fmaxf(mx, lw[s]);
+  }
   const float ref = mx == -INFINITY ? 0.f : mx;
-  float w0 = expf(l0 - ref), w1 = expf(l1 - ref);
-  float tot = w0 + w1;
-  for (int o = 16; o; o >>= 1) tot += __shfl_xor_sync(0xffffffffu, tot, o);
+  float tot = 0.f;
+#pragma unroll 8
+  for (int s = 0; s < splits; ++s) {
+    lw[s] = __expf(lw[s] - ref);
+    tot += lw[s];
+  }
   const float inv = tot > 0.f ? 1.f / tot : 0.f;
-  for (int c = lane; c < HD; c += 32) {
-    float acc = 0.f;
+  const float* base = part_o + (i * Hq + h) * HD;
+  const int64_t sstride = (int64_t)C * Hq * HD;
+  for (int c = lane * 4; c < HD; c += 128) {
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 8
     for (int s = 0; s < splits; ++s) {
-      const float wgt = __shfl_sync(0xffffffffu, s < 32 ? w0 : w1, s & 31);
-      acc += wgt * part_o[(((int64_t)s * C + i) * Hq + h) * HD + c];
+      const float4 v = __ldg(reinterpret_cast<const float4*>(base + s * sstride + c));
+      acc.x = fmaf(lw[s], v.x, acc.x);
+      acc.y = fmaf(lw[s], v.y, acc.y);
+      acc.z = fmaf(lw[s], v.z, acc.z);
+      acc.w = fmaf(lw[s], v.w, acc.w);
     }
-    out[(i * Hq + h) * HD + c] = (OutT)(acc * inv);
+    OutT* o = out + (i * Hq + h) * HD + c;
+    o[0] = (OutT)(acc.x * inv);
+    o[1] = (OutT)(acc.y * inv);
+    o[2] = (OutT)(acc.z * inv);
+    o[3] = (OutT)(acc.w * inv);
   }
   if (lse && lane == 0) lse[h * C + i] = tot > 0.f ? ref + logf(tot) : -INFINITY;
 }

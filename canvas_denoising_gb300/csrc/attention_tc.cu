@@ -28,6 +28,7 @@
 // DG_ERR_TIMEOUT, drains what it issued, frees TMEM and returns.
 #include <cudaTypedefs.h>
 #include <math.h>
+#include <stdlib.h>
 
 #include <mutex>
 
@@ -317,16 +318,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (grp_any(q, !pf)) { ok = false; break; }
         tc_fence_after();
       }
-      if (__any_sync(0xffffffffu, need)) {
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          float o[32];
-          tmem_ld32(tO + loff + c * 32, o);
-#pragma unroll
-          for (int e = 0; e < 32; ++e) o[e] *= factor;
-          tmem_st32(tO + loff + c * 32, o);
-        }
-      }
       uint8_t* prow = sm + kOffP + q * kTile + r * 128;
       const float rr = ref == -INFINITY ? 0.f : ref;
       float sum8[8];
@@ -345,6 +336,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             make_uint4(pack2(p8[0], p8[1]), pack2(p8[2], p8[3]), pack2(p8[4], p8[5]), pack2(p8[6], p8[7]));
       }
       l += ((sum8[0] + sum8[1]) + (sum8[2] + sum8[3])) + ((sum8[4] + sum8[5]) + (sum8[6] + sum8[7]));
+      // O holds every PV issued so far (waited above); rescale it before PV(jj) adds to it.
+      // Done after P is formed so the S row and the O chunk are never live together.
+      if (__any_sync(0xffffffffu, need)) {
+#pragma unroll 1
+        for (int c = 0; c < 4; ++c) {
+          float o[32];
+          tmem_ld32(tO + loff + c * 32, o);
+#pragma unroll
+          for (int e = 0; e < 32; ++e) o[e] *= factor;
+          tmem_st32(tO + loff + c * 32, o);
+        }
+      }
       tc_fence_before();
       fence_proxy_async_smem();
       mbar_arrive(smem_addr(&p_full[q]));
@@ -430,7 +433,12 @@ void attn_tc_plan(int C, int Hq, int Hkv, int64_t P, int* splits, int* tiles_per
   const int64_t base = ((M + kBM - 1) / kBM) * Hkv;
   const int nct = (int)((P + kBN - 1) / kBN), nvt = (C + kBN - 1) / kBN;
   const int tiles = nct + nvt;
-  int want = (int)(num_sms() / base);
+  static const int env_splits = [] {
+    const char* v = getenv("DG_ATTN_SPLITS");  // tuning knob: force the number of key splits
+    const int x = v ? atoi(v) : 0;
+    return x > 0 ? x : 0;
+  }();
+  int want = env_splits ? env_splits : (int)(num_sms() / base);
   if (want < 1) want = 1;
   if (want > tiles) want = tiles;
   if (want > 64) want = 64;

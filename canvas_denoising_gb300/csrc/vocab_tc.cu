@@ -562,7 +562,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 // producers is recomputed here from scratch with its true maximum as the
 // reference (fp32, CUDA cores; slow, only for rows whose logits exceed the
 // sampled reference by more than the safe margin).
-constexpr int kCombineCols = 1024;
+constexpr int kCombineCols = 1024;  // columns of S per combine CTA (4 per thread)
 
 __global__ void __launch_bounds__(256) vocab_combine(const Params p, const __nv_bfloat16* __restrict__ h,
                                                      const __nv_bfloat16* __restrict__ emb, int32_t* argmax,
@@ -571,6 +571,20 @@ __global__ void __launch_bounds__(256) vocab_combine(const Params p, const __nv_
   __shared__ float s_m[8], s_z[8], s_r[8], s_pv[256];
   __shared__ int s_a[8];
   const int i = blockIdx.x, slice = blockIdx.y, t = threadIdx.x, lane = t & 31, w = t >> 5;
+
+  // Issue this thread's partial-S loads first (4 columns x every split), so
+  // they are in flight while the row statistics are reduced below.
+  constexpr int kMaxSplitRegs = 8;
+  const int jc = slice * kCombineCols + 4 * t;
+  const bool has_cols = selfcond && jc < p.d && p.ksplit <= kMaxSplitRegs;
+  float4 part[kMaxSplitRegs];
+  if (has_cols) {
+    const float* src = p.cpart + (size_t)i * p.d + jc;
+    const size_t kstride = (size_t)256 * p.d;
+#pragma unroll
+    for (int k = 0; k < kMaxSplitRegs; ++k)
+      if (k < p.ksplit) part[k] = __ldcg(reinterpret_cast<const float4*>(src + k * kstride));
+  }
   float m = -INFINITY, z = 0.f, R = -INFINITY;
   int ai = 0x7fffffff;
   const size_t rb = (size_t)i * p.n_a;
@@ -606,15 +620,30 @@ __global__ void __launch_bounds__(256) vocab_combine(const Params p, const __nv_
     out_lse = R + logf(z);
     if (selfcond) {
       const float inv = 1.f / z;
-      for (int j = c0 + 2 * t; j < c1; j += 512) {
-        float2 acc = make_float2(0.f, 0.f);
-        for (int k = 0; k < p.ksplit; ++k) {
-          const float2 v = *reinterpret_cast<const float2*>(p.cpart + ((size_t)k * 256 + i) * p.d + j);
-          acc.x += v.x;
-          acc.y += v.y;
+      if (has_cols) {
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int k = 0; k < kMaxSplitRegs; ++k)
+          if (k < p.ksplit) {
+            acc.x += part[k].x;
+            acc.y += part[k].y;
+            acc.z += part[k].z;
+            acc.w += part[k].w;
+          }
+        __nv_bfloat162* o = reinterpret_cast<__nv_bfloat162*>(selfcond + (size_t)i * p.d + jc);
+        o[0] = __floats2bfloat162_rn(acc.x * inv, acc.y * inv);
+        o[1] = __floats2bfloat162_rn(acc.z * inv, acc.w * inv);
+      } else if (p.ksplit > kMaxSplitRegs) {
+        for (int j = c0 + 2 * t; j < c1; j += 512) {
+          float2 acc = make_float2(0.f, 0.f);
+          for (int k = 0; k < p.ksplit; ++k) {
+            const float2 v = __ldcg(reinterpret_cast<const float2*>(p.cpart + ((size_t)k * 256 + i) * p.d + j));
+            acc.x += v.x;
+            acc.y += v.y;
+          }
+          *reinterpret_cast<__nv_bfloat162*>(selfcond + (size_t)i * p.d + j) =
+              __floats2bfloat162_rn(acc.x * inv, acc.y * inv);
         }
-        *reinterpret_cast<__nv_bfloat162*>(selfcond + (size_t)i * p.d + j) =
-            __floats2bfloat162_rn(acc.x * inv, acc.y * inv);
       }
     }
   } else {
