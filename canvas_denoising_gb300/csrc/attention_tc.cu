@@ -12,7 +12,7 @@
 // first the cache rows [0, P), then the canvas rows [0, C); tiles never
 // straddle the two, and the tensor maps' row extents are exactly P and C, so
 // rows past the end read as zeros. K and V tiles stream through a 3-slot TMA
-// ring. For each key tile and each query tile q:
+// ring in the order K0 K1 V0 K2 V1 ..., keys one tile ahead of values. For each key tile and each query tile q:
 //   S_q = Q_q K^T   tcgen05 into TMEM (128 columns per query tile)
 //   softmax         4 warps per query tile, one row per thread: one 128-column
 //                   TMEM load (after which S_q may be overwritten), row max, a
@@ -21,8 +21,8 @@
 //                   P = exp2(s - ref) in bf16 into shared memory in the
 //                   128-byte-swizzled K-major operand layout
 //   O_q += P_q V    tcgen05, V read MN-major, O_q accumulated in TMEM.
-// The MMA warp interleaves the two query tiles (S0(j+1) PV0(j) S1(j+1)
-// PV1(j)), so one softmax group works while the tensor core serves the other.
+// The MMA warp issues S0(j+1) S1(j+1) PV0(j) PV1(j): both softmax groups
+// work on tile j while the tensor core computes the next scores.
 // Splits write fp32 partials (O, lse) merged by attn_combine.
 // Every wait is bounded (about two seconds); on expiry the CTA latches
 // DG_ERR_TIMEOUT, drains what it issued, frees TMEM and returns.
@@ -137,6 +137,32 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   const int n = T1 > T0 ? T1 - T0 : 0;
 
+  // Ring items in load order K0, K1, V0, K2, V1, ..., K(n-1), V(n-2), V(n-1): keys run
+  // one tile ahead of values, so the slot a key tile needs frees a whole tile early.
+  // Item index of K(j): 0 for j = 0, else 2j - 1. Item index of V(j): 2j + 2, or
+  // 2n - 1 for the last tile.
+  auto item_tile = [&](int it, bool& is_v) -> int {
+    if (it == 0) { is_v = false; return 0; }
+    if (it == 2 * n - 1) { is_v = true; return n - 1; }
+    if (it & 1) { is_v = false; return (it + 1) >> 1; }
+    is_v = true;
+    return (it >> 1) - 1;
+  };
+  auto k_item = [&](int jj) { return jj == 0 ? 0 : 2 * jj - 1; };
+  auto v_item = [&](int jj) { return jj == n - 1 ? 2 * n - 1 : 2 * jj + 2; };
+  auto issue_item = [&](int it) {
+    bool is_v;
+    const int jj = item_tile(it, is_v), t = T0 + jj;
+    const int slot = it % kRing;
+    const bool cache = t < a.n_cache_tiles;
+    const int y = cache ? t * kBN : (t - a.n_cache_tiles) * kBN;
+    const CUtensorMap* mp = cache ? (is_v ? &tv_c : &tk_c) : (is_v ? &tv_n : &tk_n);
+    mbar_expect_tx(smem_addr(&ring_full[slot]), kTile);
+    tma_load_3d(sbase + kOffRing + slot * kTile, mp, 0, y, g, smem_addr(&ring_full[slot]));
+    tma_load_3d(sbase + kOffRing + slot * kTile + kChunk, mp, 64, y, g, smem_addr(&ring_full[slot]));
+  };
+  const int n_pre = 2 * n < kRing ? 2 * n : kRing;  // ring items issued before Q is staged
+
   if (tid == 0) {
     abort_flag = 0;
     for (int s = 0; s < kRing; ++s) {
@@ -151,12 +177,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(smem_addr(&drain), 1);
     fence_mbar_init();
-    if (a.P > 0) {
-      prefetch_tmap(&tk_c);
-      prefetch_tmap(&tv_c);
-    }
-    prefetch_tmap(&tk_n);
-    prefetch_tmap(&tv_n);
+    // start the first K/V loads now, so they overlap the Q staging below
+    for (int it = 0; it < n_pre; ++it) issue_item(it);
   }
   if (warp == 1) {
     tmem_alloc(smem_addr(&tmem_slot), 512);
@@ -183,22 +205,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = tmem_slot;
 
   if (warp == 0) {
-    // ------------------------------------------------ TMA producer: K0 V0 K1 V1 ... through a 3-slot ring
+    // ------------------------------------------------ TMA producer: K0 K1 V0 K2 V1 ... through a 3-slot ring
     if (lane == 0 && n > 0) {
       bool issued[kRing] = {false, false, false};
       uint32_t par[kRing] = {0, 0, 0};
-      for (int it = 0; it < 2 * n; ++it) {
-        const int jj = it >> 1, t = T0 + jj;
-        const bool is_v = it & 1;
+      for (int it = 0; it < n_pre; ++it) issued[it] = true;  // phase 0, issued during set-up
+      for (int it = n_pre; it < 2 * n; ++it) {
         const int slot = it % kRing;
         const uint32_t ph = (uint32_t)(it / kRing) & 1u;
-        const bool cache = t < a.n_cache_tiles;
-        const int y = cache ? t * kBN : (t - a.n_cache_tiles) * kBN;
-        const CUtensorMap* mp = cache ? (is_v ? &tv_c : &tk_c) : (is_v ? &tv_n : &tk_n);
         if (!wait_bar(smem_addr(&ring_empty[slot]), ph ^ 1u, ctl)) break;
-        mbar_expect_tx(smem_addr(&ring_full[slot]), kTile);
-        tma_load_3d(sbase + kOffRing + slot * kTile, mp, 0, y, g, smem_addr(&ring_full[slot]));
-        tma_load_3d(sbase + kOffRing + slot * kTile + kChunk, mp, 64, y, g, smem_addr(&ring_full[slot]));
+        issue_item(it);
         issued[slot] = true;
         par[slot] = ph;
       }
@@ -208,12 +224,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else if (warp == 1) {
     // ------------------------------------------------ MMA issuer
-    // order: S0(0) S1(0) | S0(1) PV0(0) S1(1) PV1(0) | S0(2) PV0(1) S1(2) PV1(1) | ...
+    // order: S0(0) S1(0) | S0(1) S1(1) PV0(0) PV1(0) | S0(2) S1(2) PV0(1) PV1(1) | ...
+    // Each group's next S is issued as soon as that group has loaded its current
+    // S, so both softmax groups work on a tile at the same time.
     if (lane == 0 && n > 0) {
       const uint32_t id_s = idesc_bf16_f32(128, kBN, 0, 0);
       const uint32_t id_o = idesc_bf16_f32(128, kHD, 0, 1);
       auto issue_s = [&](int q, int jj) -> bool {
-        const int it = 2 * jj, slot = it % kRing;
+        const int it = k_item(jj), slot = it % kRing;
         if (!wait_bar(smem_addr(&ring_full[slot]), (uint32_t)(it / kRing) & 1u, ctl)) return false;
         if (jj > 0 && !wait_bar(smem_addr(&s_free[q]), (uint32_t)(jj - 1) & 1u, ctl)) return false;
         tc_fence_after();
@@ -229,7 +247,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         return true;
       };
       auto issue_pv = [&](int q, int jj) -> bool {
-        const int it = 2 * jj + 1, slot = it % kRing;
+        const int it = v_item(jj), slot = it % kRing;
         if (!wait_bar(smem_addr(&ring_full[slot]), (uint32_t)(it / kRing) & 1u, ctl)) return false;
         if (!wait_bar(smem_addr(&p_full[q]), (uint32_t)jj & 1u, ctl)) return false;
         tc_fence_after();
@@ -246,9 +264,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       };
       bool ok = issue_s(0, 0) && issue_s(1, 0);
       for (int jj = 0; jj < n && ok; ++jj) {
-        if (jj + 1 < n && !issue_s(0, jj + 1)) break;
+        if (jj + 1 < n && !(issue_s(0, jj + 1) && issue_s(1, jj + 1))) break;
         if (!issue_pv(0, jj)) break;
-        if (jj + 1 < n && !issue_s(1, jj + 1)) break;
         if (!issue_pv(1, jj)) break;
       }
       mma_commit(smem_addr(&drain));
@@ -312,17 +329,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           l *= factor;
         }
       }
-      // PV(jj-1) must be complete both before P is overwritten and before O is rescaled
-      if (jj > 0) {
-        const bool pf = wait_bar(smem_addr(&p_free[q]), (uint32_t)(jj - 1) & 1u, ctl);
-        if (grp_any(q, !pf)) { ok = false; break; }
-        tc_fence_after();
-      }
-      uint8_t* prow = sm + kOffP + q * kTile + r * 128;
+      // P row of this tile, packed to bf16 in registers while PV(jj-1) may still run
       const float rr = ref == -INFINITY ? 0.f : ref;
       float sum8[8];
 #pragma unroll
       for (int e = 0; e < 8; ++e) sum8[e] = 0.f;
+      uint32_t pk[kBN / 2];
 #pragma unroll
       for (int c = 0; c < kBN / 8; ++c) {
         float p8[8];
@@ -331,9 +343,21 @@ __global__ void __launch_bounds__(kThreads, 1)
           p8[e] = ex2_approx(fmaf(v[c * 8 + e], a.scale_log2, -rr));  // exp2(-inf) = 0 for masked keys
           sum8[e] += p8[e];
         }
+#pragma unroll
+        for (int e = 0; e < 4; ++e) pk[c * 4 + e] = pack2(p8[2 * e], p8[2 * e + 1]);
+      }
+      // PV(jj-1) must be complete both before P is overwritten and before O is rescaled
+      if (jj > 0) {
+        const bool pf = wait_bar(smem_addr(&p_free[q]), (uint32_t)(jj - 1) & 1u, ctl);
+        if (grp_any(q, !pf)) { ok = false; break; }
+        tc_fence_after();
+      }
+      uint8_t* prow = sm + kOffP + q * kTile + r * 128;
+#pragma unroll
+      for (int c = 0; c < kBN / 8; ++c) {
         const int chunk = c >> 3, piece = c & 7;
         *reinterpret_cast<uint4*>(prow + chunk * kChunk + ((piece ^ (r & 7)) << 4)) =
-            make_uint4(pack2(p8[0], p8[1]), pack2(p8[2], p8[3]), pack2(p8[4], p8[5]), pack2(p8[6], p8[7]));
+            make_uint4(pk[c * 4], pk[c * 4 + 1], pk[c * 4 + 2], pk[c * 4 + 3]);
       }
       l += ((sum8[0] + sum8[1]) + (sum8[2] + sum8[3])) + ((sum8[4] + sum8[5]) + (sum8[6] + sum8[7]));
       // O holds every PV issued so far (waited above); rescale it before PV(jj) adds to it.
