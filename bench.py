@@ -48,6 +48,7 @@ def parse():
     ap.add_argument("--workload", default=HEADLINE, choices=sorted(WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-graph", action="store_true", help="launch every kernel from Python instead of a CUDA graph")
     return ap.parse_args()
 
 
@@ -56,6 +57,25 @@ def dist_env():
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     return world, rank, local
+
+
+def replica_seed(base_seed: int, rank: int) -> int:
+    """Replicas: every rank denoises its own canvas, seeded by its rank."""
+    return base_seed + rank
+
+
+def max_over_ranks(value: float, device=None) -> float:
+    """Slowest rank's time (the job finishes when the last replica does)."""
+    if not (torch.distributed.is_available() and torch.distributed.is_initialized()):
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_rate(world: int, steps: int, ms: float) -> float:
+    """Whole-job steps/s: every rank ran `steps` steps; time is the slowest rank's."""
+    return world * steps / (ms / 1e3)
 
 
 def metric_name():
@@ -183,14 +203,13 @@ class Canvas:
         n += 2 if self.ws_attn.numel() > 256 else 1
         if ev is not None:
             ev[0].record(stream)
-        B.vocab_step(h, self.emb, argmax=self.argmax, conf=self.conf, lse=self.lse, selfcond=self.selfcond,
-                     workspace=self.ws_vocab, stream=stream)
+        # vocabulary step with the threshold re-noise fused into its last kernel
+        B.vocab_step_renoise(h, self.emb, self.tokens, w.thresholds[0], self.seed, j, self.P, argmax=self.argmax,
+                             conf=self.conf, lse=self.lse, selfcond=self.selfcond, renoised=self.renoised,
+                             workspace=self.ws_vocab, stream=stream)
         if ev is not None:
             ev[1].record(stream)
         n += 2
-        B.renoise(self.tokens, self.argmax, self.conf, w.V, w.thresholds[0], self.seed, j, self.P,
-                  renoised=self.renoised, stream=stream)
-        n += 1
         if j == w.steps - 1:
             # finished canvas -> cache rows [P, P+C); the next canvas restarts at the same prefix
             B.kv_append(self.k, self.v, self.P, kn, vn, stream=stream)
@@ -209,7 +228,7 @@ def run_ours(args, world, rank, local):
     if not os.path.exists(build_mod.LIB):
         raise SystemExit("libdgcanvas is not built: run `python -c 'import __graft_entry__ as g; g.build()'` first")
     B.load()
-    seed = w.seed + rank  # replicas: every rank denoises its own canvas
+    seed = replica_seed(w.seed, rank)
     cv = Canvas(w, seed, dev)
     stream = torch.cuda.Stream(device=dev)
     torch.cuda.synchronize()
@@ -221,7 +240,10 @@ def run_ours(args, world, rank, local):
         raise SystemExit("device status error after warm-up")
 
     K = args.steps
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    spc = w.steps  # one CUDA graph = one canvas: init, `spc` steps, append
+    graph, g_evs, g_launches = None, None, 0
+    if not args.no_graph:
+        graph, g_evs, g_launches = capture_canvas_graph(cv, stream, spc)
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     clocks = ClockSampler(local)
     if world > 1:
@@ -230,23 +252,28 @@ def run_ours(args, world, rank, local):
     clocks.start()
     time.sleep(0.3)
     launches = 0
+    replays = K // spc if graph is not None else 0
+    eager = K - replays * spc
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(eager)]
     with torch.cuda.stream(stream):
         t0.record(stream)
-        for s in range(K):
-            launches += cv.step(args.warmup + s, stream, ev=evs[s])
+        for _ in range(replays):
+            graph.replay()
+            launches += g_launches
+        for s in range(eager):
+            launches += cv.step(s, stream, ev=evs[s])
         t1.record(stream)
     stream.synchronize()
     torch.cuda.synchronize()
     clk = clocks.stop()
+    if replays:
+        evs = list(g_evs) + evs  # the event nodes hold the last replay's times
     if world > 1:
         torch.distributed.barrier()
     ms = t0.elapsed_time(t1)
     status = B.device_status(stream)
     vocab_ms = statistics.mean(a.elapsed_time(b) for a, b in evs)
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(ms, dev)
 
     # ---- end to end through the public API: per-step inputs from pinned host memory, result back
     e2e = None
@@ -273,11 +300,8 @@ def run_ours(args, world, rank, local):
             e1.record(stream)
         stream.synchronize()
         ems = e0.elapsed_time(e1)
-        if world > 1:
-            t = torch.tensor([ems], device=dev)
-            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-            ems = float(t.item())
-        e2e = {"value": round(world * Ke / (ems / 1e3), 3), "unit": "steps/s", "h2d_bytes_per_step": int(h2d),
+        ems = max_over_ranks(ems, dev)
+        e2e = {"value": round(job_rate(world, Ke, ems), 3), "unit": "steps/s", "h2d_bytes_per_step": int(h2d),
                "d2h_bytes_per_step": int(d2h), "steps": Ke}
 
     if rank != 0:
@@ -288,12 +312,12 @@ def run_ours(args, world, rank, local):
     flops = 4.0 * w.C * w.V * w.d
     achieved = flops / (vocab_ms / 1e3) / 1e12
     traffic = committed_traffic("vocab_main", args.workload)
-    roof = {"kernel": "dg_vocab_step (vocab_main + vocab_combine)", "bound": "tensor",
+    roof = {"kernel": "dg_vocab_step_renoise (vocab_main + vocab_combine)", "bound": "tensor",
             "achieved": round(achieved, 1), "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
             "frac": round(achieved / pk["bf16_tflops"], 4), "traffic": traffic,
             "peak_source": f"{pk['source']} bf16 burst", "algorithmic_flops_per_launch": flops,
             "avg_launch_ms": round(vocab_ms, 4)}
-    steps_per_s = world * K / (ms / 1e3)
+    steps_per_s = job_rate(world, K, ms)
     line = {
         "metric": metric_name(), "value": round(steps_per_s, 3), "unit": "steps/s", "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": round(ms / K, 5), "higher_is_better": True, "scaling": "weak",
@@ -305,6 +329,7 @@ def run_ours(args, world, rank, local):
                    "l2": "inputs larger than L2 (embedding table %.2f GB), no flush" % (w.V * w.d * 2 / 1e9)},
         "roofline": roof,
         "gpu_launches": launches * world,
+        "cuda_graph": bool(replays), 
         "clocks": clk, "device_status": status,
     }
     if e2e is not None:
@@ -314,6 +339,32 @@ def run_ours(args, world, rank, local):
     if world > 1:
         torch.distributed.destroy_process_group()
     return line
+
+
+def capture_canvas_graph(cv, stream, spc):
+    """Captures one canvas (init, spc denoising steps, append) as a CUDA graph,
+    with timing events around each vocabulary step as event nodes. Returns
+    (graph, events, kernel launches per replay), or (None, None, 0) if this
+    torch cannot record timing events inside a graph."""
+    try:
+        evs = [(torch.cuda.Event(enable_timing=True, external=True),
+                torch.cuda.Event(enable_timing=True, external=True)) for _ in range(spc)]
+    except TypeError:
+        return None, None, 0
+    g = torch.cuda.CUDAGraph()
+    n = 0
+    try:
+        with torch.cuda.graph(g, stream=stream):
+            for j in range(spc):
+                n += cv.step(j, stream, ev=evs[j])
+    except Exception as e:  # e.g. a launch kind this driver cannot capture: fall back to eager launches
+        print(f"CUDA graph capture failed ({e}); timing eager launches", file=sys.stderr)
+        torch.cuda.synchronize()
+        return None, None, 0
+    stream.synchronize()
+    g.replay()  # one untimed replay
+    stream.synchronize()
+    return g, evs, n
 
 
 def committed_traffic(kernel, workload):

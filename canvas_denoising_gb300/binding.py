@@ -36,6 +36,8 @@ _SIGS = {
     "dg_canvas_attn_noalloc_max_scratch": (_c_sz, []),
     "dg_vocab_step_workspace_size": (_c_sz, [_c_int, _c_int, _c_int, _c_int]),
     "dg_vocab_step": (_c_int, [_p, _p, _c_int, _c_int, _c_int, _c_int, _p, _p, _p, _p, _p, _c_sz, _p]),
+    "dg_vocab_step_renoise": (_c_int, [_p, _p, _c_int, _c_int, _c_int, _c_int, _p, _p, _p, _p, _p, _c_f, _c_u64,
+                                       _c_u32, _c_i64, _p, _p, _c_sz, _p]),
     "dg_renoise": (_c_int, [_p, _p, _p, _c_int, _c_int, _c_f, _c_u64, _c_u32, _c_i64, _p, _p]),
     "dg_canvas_init": (_c_int, [_p, _c_int, _c_int, _c_u64, _c_i64, _p]),
     "dg_kv_append": (_c_int, [_p, _p, _c_i64, ctypes.POINTER(_c_i64), _p, _p, _c_int, _c_int, _c_int, _c_int, _p,
@@ -186,6 +188,31 @@ def vocab_step(h, emb, argmax=None, conf=None, lse=None, selfcond=None, workspac
     rc = load().dg_vocab_step(_ptr(h), _ptr(emb), C, V, d, dt, _ptr(argmax), _ptr(conf), _ptr(lse), _ptr(selfcond),
                               _ptr(workspace), ws_bytes, _stream(stream))
     _check("dg_vocab_step", rc)
+    return argmax, conf, lse, selfcond
+
+
+def vocab_step_renoise(h, emb, tokens, threshold, seed, step, abs_pos0, argmax=None, conf=None, lse=None,
+                       selfcond=None, renoised=None, workspace=None, stream=None):
+    """dg_vocab_step and dg_renoise in one call (re-noise fused into the last kernel)."""
+    _need(h, "h")
+    _need(emb, "emb")
+    _need(tokens, "tokens")
+    C, d = h.shape
+    V = emb.shape[0]
+    dt = _dtype_code(h)
+    dev = h.device
+    argmax = torch.empty(C, dtype=torch.int32, device=dev) if argmax is None else argmax
+    conf = torch.empty(C, dtype=torch.float32, device=dev) if conf is None else conf
+    lse = torch.empty(C, dtype=torch.float32, device=dev) if lse is None else lse
+    selfcond = torch.empty((C, d), dtype=h.dtype, device=dev) if selfcond is None else selfcond
+    need = vocab_step_workspace_size(C, V, d, dt)
+    if workspace is None and need:
+        workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    rc = load().dg_vocab_step_renoise(_ptr(h), _ptr(emb), C, V, d, dt, _ptr(argmax), _ptr(conf), _ptr(lse),
+                                      _ptr(selfcond), _ptr(tokens), float(threshold), seed, step, abs_pos0,
+                                      _ptr(renoised), _ptr(workspace), ws_bytes, _stream(stream))
+    _check("dg_vocab_step_renoise", rc)
     return argmax, conf, lse, selfcond
 
 

@@ -99,3 +99,25 @@ extern "C" int dg_vocab_step(const void* h, const void* emb, int C, int V, int d
   return vocab_tc_launch((const __nv_bfloat16*)h, (const __nv_bfloat16*)emb, C, V, d, argmax, conf, lse,
                          (__nv_bfloat16*)selfcond, workspace, workspace_bytes, s);
 }
+
+extern "C" int dg_vocab_step_renoise(const void* h, const void* emb, int C, int V, int d, int dtype, int32_t* argmax,
+                                     float* conf, float* lse, void* selfcond, int32_t* tokens, float threshold,
+                                     uint64_t seed, uint32_t step, int64_t abs_pos0, uint8_t* renoised,
+                                     void* workspace, size_t workspace_bytes, void* stream) {
+  if (!tokens || abs_pos0 < 0 || threshold != threshold) return DG_ERR_INVALID_ARG;
+  if (dtype != DG_BF16) {
+    // CUDA-core path: the two calls back to back
+    const int rc = dg_vocab_step(h, emb, C, V, d, dtype, argmax, conf, lse, selfcond, workspace, workspace_bytes,
+                                 stream);
+    if (rc != DG_OK) return rc;
+    return dg_renoise(tokens, argmax, conf, C, V, threshold, seed, step, abs_pos0, renoised, stream);
+  }
+  if (!h || !emb || !argmax || !conf || C < 1 || V < 1 || d < 1) return DG_ERR_INVALID_ARG;
+  if (C > 256 || d % 64 || d > 8192) return DG_ERR_UNSUPPORTED;
+  if (!aligned16(h) || !aligned16(emb) || (selfcond && !aligned16(selfcond))) return DG_ERR_INVALID_ARG;
+  if (workspace_bytes < vocab_tc_workspace(C, V, d)) return DG_ERR_WORKSPACE;
+  if (vocab_tc_workspace(C, V, d) && ((uintptr_t)workspace & 255u)) return DG_ERR_INVALID_ARG;
+  RenoiseArgs rn{tokens, renoised, threshold, seed, step, abs_pos0};
+  return vocab_tc_launch((const __nv_bfloat16*)h, (const __nv_bfloat16*)emb, C, V, d, argmax, conf, lse,
+                         (__nv_bfloat16*)selfcond, workspace, workspace_bytes, (cudaStream_t)stream, &rn);
+}

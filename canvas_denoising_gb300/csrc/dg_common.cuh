@@ -78,8 +78,18 @@ int attn_tc_launch(const void* q, const void* k_cache, const void* v_cache, int6
 int vocab_simt_launch(const float* h, const float* emb, int C, int V, int d, int32_t* argmax, float* conf,
                       float* lse, float* selfcond, cudaStream_t s);
 
+struct RenoiseArgs {  // threshold re-noise fused into the vocabulary step's last kernel
+  int32_t* tokens;
+  uint8_t* renoised;
+  float threshold;
+  uint64_t seed;
+  uint32_t step;
+  int64_t abs_pos0;
+};
+
 size_t vocab_tc_workspace(int C, int V, int d);
 int vocab_tc_launch(const __nv_bfloat16* h, const __nv_bfloat16* emb, int C, int V, int d, int32_t* argmax,
-                    float* conf, float* lse, __nv_bfloat16* selfcond, void* ws, size_t ws_bytes, cudaStream_t s);
+                    float* conf, float* lse, __nv_bfloat16* selfcond, void* ws, size_t ws_bytes, cudaStream_t s,
+                    const RenoiseArgs* rn = nullptr);
 
 }  // namespace dg

@@ -158,6 +158,13 @@ struct Params {
   float* az;       // [256][n_a] sum of exp(l - R)
   float* cpart;    // [ksplit][256][d]
   uint8_t* pbuf;   // [n_vt][4 sub-tiles of 64 ids][n_rh][16 KB]
+  // optional fused threshold re-noise (tokens == nullptr: off)
+  int32_t* rn_tokens;
+  uint8_t* rn_flags;
+  float rn_threshold;
+  uint64_t rn_seed;
+  uint32_t rn_step;
+  int64_t rn_pos0;
   int* status;
 };
 
@@ -694,6 +701,12 @@ __global__ void __launch_bounds__(256) vocab_combine(const Params p, const __nv_
     argmax[i] = ai;
     conf[i] = out_conf;
     if (lse) lse[i] = out_lse;
+    if (p.rn_tokens) {
+      // threshold re-noise of this position (same rule and draw as dg_renoise)
+      const bool low = out_conf < p.rn_threshold;
+      p.rn_tokens[i] = low ? uniform_token(p.rn_seed, p.rn_step, p.rn_pos0 + i, kDomainRenoise, (uint32_t)p.V) : ai;
+      if (p.rn_flags) p.rn_flags[i] = low ? 1 : 0;
+    }
   }
 }
 
@@ -713,7 +726,8 @@ size_t vocab_tc_workspace(int C, int V, int d) {
 }
 
 int vocab_tc_launch(const __nv_bfloat16* h, const __nv_bfloat16* emb, int C, int V, int d, int32_t* argmax,
-                    float* conf, float* lse, __nv_bfloat16* selfcond, void* ws, size_t ws_bytes, cudaStream_t s) {
+                    float* conf, float* lse, __nv_bfloat16* selfcond, void* ws, size_t ws_bytes, cudaStream_t s,
+                    const RenoiseArgs* rn) {
   const Plan pl = make_plan(C, V, d);
   const Layout L = make_layout(pl, d);
   if (ws_bytes < L.total) return DG_ERR_WORKSPACE;
@@ -744,6 +758,12 @@ int vocab_tc_launch(const __nv_bfloat16* h, const __nv_bfloat16* emb, int C, int
   p.cpart = (float*)(w + L.cpart);
   p.pbuf = w + L.pbuf;
   p.status = st;
+  p.rn_tokens = rn ? rn->tokens : nullptr;
+  p.rn_flags = rn ? rn->renoised : nullptr;
+  p.rn_threshold = rn ? rn->threshold : 0.f;
+  p.rn_seed = rn ? rn->seed : 0;
+  p.rn_step = rn ? rn->step : 0;
+  p.rn_pos0 = rn ? rn->abs_pos0 : 0;
   DG_CUDA_TRY(cudaMemsetAsync(flags, 0, L.flag_bytes, s));
 
   const size_t smem = (size_t)kStages * kStageBytes + 1024;

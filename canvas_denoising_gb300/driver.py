@@ -3,9 +3,9 @@ denoise a 256-token canvas for a fixed number of steps, append the finished
 canvas to the KV cache by incremental causal prefill, start the next canvas.
 
 Each step runs, on one stream and entirely in libdgcanvas kernels:
-  dg_canvas_attn   bidirectional attention of the canvas over cache + canvas
-  dg_vocab_step    logits, softmax, argmax, confidence, self-conditioning
-  dg_renoise       threshold re-noise of low-confidence positions
+  dg_canvas_attn         bidirectional attention of the canvas over cache + canvas
+  dg_vocab_step_renoise  logits, softmax, argmax, confidence, self-conditioning,
+                         and the threshold re-noise of low-confidence positions
 and each canvas starts with dg_canvas_init and ends with dg_kv_append.
 
 The backbone that turns tokens into Q/K/V and the final hidden state is not
@@ -71,10 +71,10 @@ class CanvasDenoiser:
         o = self.out
         B.canvas_attn(q, self.k_cache, self.v_cache, self.len, k_canvas, v_canvas, out=o.attn_out, lse=o.attn_lse,
                       workspace=self.ws_attn, stream=self.stream)
-        B.vocab_step(h, self.emb, argmax=o.argmax, conf=o.conf, lse=o.lse, selfcond=o.selfcond,
-                     workspace=self.ws_vocab, stream=self.stream)
-        B.renoise(self.tokens, o.argmax, o.conf, self.V, self.threshold, self.seed, step, self.len,
-                  renoised=o.renoised, stream=self.stream)
+        # vocabulary step with the threshold re-noise fused into its last kernel
+        B.vocab_step_renoise(h, self.emb, self.tokens, self.threshold, self.seed, step, self.len, argmax=o.argmax,
+                             conf=o.conf, lse=o.lse, selfcond=o.selfcond, renoised=o.renoised,
+                             workspace=self.ws_vocab, stream=self.stream)
         return o
 
     def end_canvas(self, k_final, v_final, q_final=None):

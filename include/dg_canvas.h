@@ -137,6 +137,15 @@ DG_API int dg_vocab_step(const void* h, const void* emb, int C, int V, int d, in
                   int32_t* argmax, float* conf, float* lse, void* selfcond,
                   void* workspace, size_t workspace_bytes, void* stream);
 
+/* dg_vocab_step followed by dg_renoise on its argmax/conf, with the re-noise
+ * done inside the vocabulary step's last kernel (one launch fewer per step).
+ * Arguments and results are those of the two calls; tokens/renoised as in
+ * dg_renoise (step, seed, abs_pos0 key the Philox draw). */
+DG_API int dg_vocab_step_renoise(const void* h, const void* emb, int C, int V, int d, int dtype,
+                                 int32_t* argmax, float* conf, float* lse, void* selfcond,
+                                 int32_t* tokens, float threshold, uint64_t seed, uint32_t step, int64_t abs_pos0,
+                                 uint8_t* renoised, void* workspace, size_t workspace_bytes, void* stream);
+
 /* ---------------------------------------------------------------- re-noise
  * tokens[i] = conf[i] < threshold ? U(seed, step, abs_pos0 + i) : argmax[i]
  * renoised[i] = (conf[i] < threshold)            (renoised may be NULL)

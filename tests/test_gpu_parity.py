@@ -127,6 +127,21 @@ def test_canvas_attn_late_dominant_key(lib, mask):
     _status_ok()
 
 
+@pytest.mark.parametrize("name", ["v262k_d2816_p4k", "v262k_d2816_p32k"])
+def test_canvas_attn_full_size_sampled_rows(lib, name):
+    """The headline and long-context shapes, in the launch configuration the
+    benchmark uses (bidirectional); the oracle checks sampled canvas rows."""
+    w = WORKLOADS[name]
+    k, v = synth.kv_prefix(w.Hkv, w.prefix + w.C, w.hd, w.prefix, w.seed, device="cuda")
+    q, kn, vn = synth.canvas_qkv(w.C, w.Hq, w.Hkv, w.hd, w.seed, device="cuda")
+    out, lse = B.canvas_attn(q, k, v, w.prefix, kn, vn)
+    _status_ok()
+    rows = np.array([0, 1, 77, 128, 200, 255])
+    ro, rl = oracle.canvas_attention(_np(q)[rows], _np(k), _np(v), w.prefix, _np(kn), _np(vn))
+    assert_rows_close(_np(out)[rows].reshape(-1, w.hd), ro.reshape(-1, w.hd), what="attn out")
+    assert np.abs(_np(lse)[:, rows] - rl).max() <= LSE_ABS
+
+
 def test_canvas_attn_f32_tiny(lib):
     w = WORKLOADS["tiny_f32"]
     k, v = synth.kv_prefix(w.Hkv, w.cap, w.hd, w.prefix, w.seed, dtype=torch.float32)
@@ -205,6 +220,26 @@ def test_vocab_step_overflow_row_is_recomputed(lib):
     ref = oracle.vocab_step(_np(h), _np(emb))
     assert _np(res[0])[0] == 39000
     _check_vocab(h, emb, res, ref)
+
+
+@pytest.mark.parametrize("C,V,d,alpha,std,thr", [(256, 32768, 1024, 26.0, 0.02, 0.5), (200, 9000, 320, 2.0, 0.1, 0.1)])
+def test_vocab_step_renoise_fused_equals_two_calls(lib, C, V, d, alpha, std, thr):
+    """The fused entry point gives the same bits as dg_vocab_step + dg_renoise."""
+    h, emb = _vocab_case(C, V, d, seed=3, alpha=alpha, std=std)
+    hd, ed = h.cuda(), emb.cuda()
+    am, conf, lse, sc = B.vocab_step(hd, ed)
+    tok_ref = torch.empty(C, dtype=torch.int32, device="cuda")
+    rn_ref = torch.empty(C, dtype=torch.uint8, device="cuda")
+    B.renoise(tok_ref, am, conf, V, thr, 77, 3, 512, renoised=rn_ref)
+    tok = torch.full((C,), -1, dtype=torch.int32, device="cuda")
+    rn = torch.empty(C, dtype=torch.uint8, device="cuda")
+    am2, conf2, lse2, sc2 = B.vocab_step_renoise(hd, ed, tok, thr, 77, 3, 512, renoised=rn)
+    for x, y in ((am, am2), (conf, conf2), (lse, lse2), (sc, sc2), (tok_ref, tok), (rn_ref, rn)):
+        assert torch.equal(x, y)
+    ref = oracle.vocab_step(_np(h), _np(emb))
+    ref_tok, _ = oracle.renoise(ref["argmax"], ref["conf"].astype(np.float32), V, thr, 77, 3, 512)
+    assert ((_np(tok) == ref_tok) | decision_flags(ref, thr)).all()
+    _status_ok()
 
 
 def test_vocab_step_f32_tiny(lib):
