@@ -35,6 +35,7 @@ _SIGS = {
                                         _c_f, _c_int, _c_int, _p]),
     "dg_canvas_attn_noalloc_max_scratch": (_c_sz, []),
     "dg_vocab_step_workspace_size": (_c_sz, [_c_int, _c_int, _c_int, _c_int]),
+    "dg_vocab_step_plan": (_c_int, [_c_int, _c_int, _c_int, _c_int, _p]),
     "dg_vocab_step": (_c_int, [_p, _p, _c_int, _c_int, _c_int, _c_int, _p, _p, _p, _p, _p, _c_sz, _p]),
     "dg_vocab_step_renoise": (_c_int, [_p, _p, _c_int, _c_int, _c_int, _c_int, _p, _p, _p, _p, _p, _c_f, _c_u64,
                                        _c_u32, _c_i64, _p, _p, _c_sz, _p]),
@@ -165,6 +166,13 @@ def canvas_attn_noalloc(q, k_cache, v_cache, prefix_len, k_canvas, v_canvas, out
 # ------------------------------------------------------------------ vocabulary step
 def vocab_step_workspace_size(C, V, d, dtype=DG_BF16) -> int:
     return load().dg_vocab_step_workspace_size(C, V, d, dtype)
+
+
+def vocab_step_plan(C, V, d, dtype=DG_BF16) -> dict:
+    """The launch plan dg_vocab_step uses on the current device."""
+    buf = (ctypes.c_int32 * 6)()
+    _check("dg_vocab_step_plan", load().dg_vocab_step_plan(C, V, d, dtype, ctypes.cast(buf, ctypes.c_void_p)))
+    return dict(zip(("producers", "consumers", "vocab_split", "cluster_pairs", "ctas", "vocab_tiles"), list(buf)))
 
 
 def vocab_step(h, emb, argmax=None, conf=None, lse=None, selfcond=None, workspace=None, want_selfcond=True,

@@ -121,3 +121,8 @@ extern "C" int dg_vocab_step_renoise(const void* h, const void* emb, int C, int 
   return vocab_tc_launch((const __nv_bfloat16*)h, (const __nv_bfloat16*)emb, C, V, d, argmax, conf, lse,
                          (__nv_bfloat16*)selfcond, workspace, workspace_bytes, (cudaStream_t)stream, &rn);
 }
+
+extern "C" int dg_vocab_step_plan(int C, int V, int d, int dtype, int32_t* plan) {
+  if (!plan || dtype != DG_BF16 || C < 1 || C > 256 || V < 1 || d < 64 || d % 64 || d > 8192) return DG_ERR_INVALID_ARG;
+  return vocab_tc_plan(C, V, d, plan);
+}

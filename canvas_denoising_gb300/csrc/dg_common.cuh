@@ -88,6 +88,7 @@ struct RenoiseArgs {  // threshold re-noise fused into the vocabulary step's las
 };
 
 size_t vocab_tc_workspace(int C, int V, int d);
+int vocab_tc_plan(int C, int V, int d, int* out);
 int vocab_tc_launch(const __nv_bfloat16* h, const __nv_bfloat16* emb, int C, int V, int d, int32_t* argmax,
                     float* conf, float* lse, __nv_bfloat16* selfcond, void* ws, size_t ws_bytes, cudaStream_t s,
                     const RenoiseArgs* rn = nullptr);

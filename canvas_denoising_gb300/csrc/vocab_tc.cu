@@ -720,6 +720,17 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows, ui
 
 }  // namespace
 
+int vocab_tc_plan(int C, int V, int d, int* out) {
+  const Plan pl = make_plan(C, V, d);
+  out[0] = pl.n_a;
+  out[1] = pl.n_c;
+  out[2] = pl.ksplit;
+  out[3] = 0;  // producers are independent CTAs
+  out[4] = pl.n_a + pl.n_c;
+  out[5] = pl.n_vt;
+  return DG_OK;
+}
+
 size_t vocab_tc_workspace(int C, int V, int d) {
   Plan pl = make_plan(C, V, d);
   return make_layout(pl, d).total;

@@ -40,6 +40,7 @@ def main():
                 torch.empty(a.C, device=dev), torch.empty((a.C, a.d), dtype=torch.bfloat16, device=dev)]
         run = lambda: B.vocab_step(h, emb, *outs, workspace=ws, stream=s)
         flops = 4.0 * a.C * a.V * a.d
+        print(json.dumps({"vocab_plan": B.vocab_step_plan(a.C, a.V, a.d)}))
     elif a.op in ("attn", "append"):
         k, v = synth.kv_prefix(a.Hkv, a.P + a.C, a.hd, a.P, 0, device=dev)
         q, kn, vn = synth.canvas_qkv(a.C, a.Hq, a.Hkv, a.hd, 0, device=dev)

@@ -146,6 +146,12 @@ DG_API int dg_vocab_step_renoise(const void* h, const void* emb, int C, int V, i
                                  int32_t* tokens, float threshold, uint64_t seed, uint32_t step, int64_t abs_pos0,
                                  uint8_t* renoised, void* workspace, size_t workspace_bytes, void* stream);
 
+/* Launch plan of the bf16 vocabulary step on the current device (host-only
+ * query, no kernel): plan[0] producer CTAs, [1] consumer CTAs, [2] vocabulary
+ * split of the consumers, [3] 1 if producers run as cluster pairs sharing E by
+ * multicast, [4] CTAs launched, [5] vocabulary tiles of 256 ids. */
+DG_API int dg_vocab_step_plan(int C, int V, int d, int dtype, int32_t* plan /* [6] */);
+
 /* ---------------------------------------------------------------- re-noise
  * tokens[i] = conf[i] < threshold ? U(seed, step, abs_pos0 + i) : argmax[i]
  * renoised[i] = (conf[i] < threshold)            (renoised may be NULL)

@@ -99,3 +99,12 @@ def test_vocab_step_rejects_bad_arguments(lib):
     assert lib.dg_vocab_step(*a) == B.DG_ERR_INVALID_ARG
     a = list(base); a[5] = 7
     assert lib.dg_vocab_step(*a) == B.DG_ERR_INVALID_ARG
+
+
+def test_vocab_plan_is_a_host_query(lib):
+    import ctypes
+    buf = (ctypes.c_int32 * 6)()
+    assert lib.dg_vocab_step_plan(256, 262144, 2816, B.DG_BF16, ctypes.cast(buf, ctypes.c_void_p)) == B.DG_OK
+    n_a, n_c, ks, pair, grid, n_vt = list(buf)
+    assert n_vt == 1024 and n_c % 11 == 0 and n_c // 11 == ks and n_a + n_c <= grid <= n_a + n_c + 1
+    assert lib.dg_vocab_step_plan(256, 262144, 2800, B.DG_BF16, ctypes.cast(buf, ctypes.c_void_p)) == B.DG_ERR_INVALID_ARG
