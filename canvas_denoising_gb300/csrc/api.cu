@@ -1,5 +1,8 @@
 // C-ABI entry points that are not kernels' own files: status handling,
 // argument validation and dispatch for dg_canvas_attn and dg_vocab_step.
+#include <stdio.h>
+#include <stdlib.h>
+
 #include <mutex>
 
 #include "dg_common.cuh"
@@ -21,6 +24,14 @@ int* status_ptr() {
     addr[dev] = (int*)p;
   }
   return addr[dev];
+}
+
+void report_cuda_error(cudaError_t e, const char* what, const char* file, int line) {
+  static const bool verbose = [] {
+    const char* v = getenv("DG_VERBOSE");
+    return v && *v && *v != '0';
+  }();
+  if (verbose) fprintf(stderr, "libdgcanvas: %s failed: %s (%s:%d)\n", what, cudaGetErrorString(e), file, line);
 }
 
 }  // namespace dg

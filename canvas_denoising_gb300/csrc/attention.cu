@@ -433,8 +433,8 @@ int attn_combine_launch(const float* part_o, const float* part_lse, __nv_bfloat1
 
 size_t attn_workspace(int C, int Hq, int Hkv, int hd, int64_t P, int dtype) {
   if (dtype != DG_BF16 || C < 1 || Hkv < 1 || Hq % Hkv) return 0;
+  if (hd == 128) return attn_tc_workspace(C, Hq, Hkv, P);
   Plan pl = make_plan(C, Hq, Hkv, P);
-  if (hd == 128) attn_tc_plan(C, Hq, Hkv, P, &pl.splits, nullptr);
   if (pl.splits <= 1) return 0;
   size_t o = (size_t)pl.splits * C * Hq * hd * sizeof(float);
   o = (o + 255) & ~(size_t)255;

@@ -11,19 +11,29 @@
 // head-in-group), so a K/V tile feeds all of them. Keys come in tiles of 128:
 // first the cache rows [0, P), then the canvas rows [0, C); tiles never
 // straddle the two, and the tensor maps' row extents are exactly P and C, so
-// rows past the end read as zeros. K and V tiles stream through a 3-slot TMA
-// ring in the order K0 K1 V0 K2 V1 ..., keys one tile ahead of values. For each key tile and each query tile q:
-//   S_q = Q_q K^T   tcgen05 into TMEM (128 columns per query tile)
-//   softmax         4 warps per query tile, one row per thread: one 128-column
-//                   TMEM load (after which S_q may be overwritten), row max, a
-//                   per-row reference kept unless a tile's max exceeds it by
-//                   2^8 (then O_q and the row sum are rescaled through TMEM),
-//                   P = exp2(s - ref) in bf16 into shared memory in the
-//                   128-byte-swizzled K-major operand layout
-//   O_q += P_q V    tcgen05, V read MN-major, O_q accumulated in TMEM.
-// The MMA warp issues S0(j+1) S1(j+1) PV0(j) PV1(j): both softmax groups
-// work on tile j while the tensor core computes the next scores.
-// Splits write fp32 partials (O, lse) merged by attn_combine.
+// rows past the end read as zeros. K and V tiles stream through a 4-slot TMA
+// ring in the order K0 V0 K1 V1 ...
+//
+// Tensor memory (512 columns): S_q / P_q at 128 q, O_q at 256 + 128 q.
+// For each key tile j and query tile q:
+//   S_q = Q_q K^T     tcgen05, both operands in shared memory, fp32 in TMEM
+//   softmax           4 warps per query tile, one row per thread: the row's
+//                     max from one 128-column TMEM load, a per-row reference
+//                     kept unless a tile's max exceeds it by 2^8 (then O_q and
+//                     the row sum are rescaled in TMEM), then P = exp2(s - ref)
+//                     from a second read in 32-column chunks, packed to bf16
+//                     and written back over the first 64 columns of S_q
+//   O_q += P_q V      tcgen05 with A = P_q read from TMEM, V MN-major in smem
+// The MMA warp issues PV_0(j) S_0(j+1) PV_1(j) S_1(j+1): while one softmax
+// group works, the tensor core runs the other group's two products. Keeping P
+// in TMEM leaves shared-memory bandwidth to the S operands and the TMA ring.
+//
+// Split merge (no second kernel; the launch is cooperative, so every CTA is
+// resident): each CTA stages its normalised O rows (bf16) and per-row lse in
+// shared memory, copies them to its slot of the workspace with coalesced
+// stores, and arrives on its (row block, KV head) counter. Once all splits
+// of the group have arrived, CTA k merges rows [k*ceil(256/splits), ...) with
+// weights exp(lse_s - lse) and writes the bf16 output and the final lse.
 // Every wait is bounded (about two seconds); on expiry the CTA latches
 // DG_ERR_TIMEOUT, drains what it issued, frees TMEM and returns.
 #include <cudaTypedefs.h>
@@ -46,12 +56,14 @@ constexpr int kHD = 128;
 constexpr int kBM = 256;  // two query tiles of 128 rows
 constexpr int kBN = 128;
 constexpr int kThreads = 320;  // warp 0: TMA, warp 1: MMA, warps 2..5 / 6..9: softmax of query tile 0 / 1
-constexpr int kRing = 3;       // K/V tile slots (K0 V0 K1 V1 ... in order)
+constexpr int kRing = 4;       // K/V tile slots (K0 V0 K1 V1 ... in order)
+constexpr int kMaxSplits = 64;
 constexpr uint32_t kChunk = 16384;  // [128 rows x 64 bf16] swizzled block
 constexpr uint32_t kTile = 2 * kChunk;
-// shared memory: Q[2] | ring[3] | P[2]
-constexpr uint32_t kOffQ = 0, kOffRing = 2 * kTile, kOffP = 5 * kTile, kSmem = 7 * kTile;
-constexpr float kRescale = 8.f;  // log2 units
+// shared memory: Q[2] | ring[4]; after the last MMA it holds the staged O rows
+constexpr uint32_t kOffQ = 0, kOffRing = 2 * kTile, kSmem = kOffRing + kRing * kTile;
+constexpr uint32_t kStageRow = kHD * 2;  // bf16 O row in the merge staging area
+constexpr float kRescale = 8.f;          // log2 units
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr long long kTimeoutCycles = 4000000000ll;
 
@@ -59,13 +71,15 @@ struct TcArgs {
   const __nv_bfloat16* q;
   __nv_bfloat16* out;
   float* lse;
-  float* part_o;
-  float* part_lse;
   int C, Hq, Hkv, grp;
   int64_t P;
   int n_cache_tiles, n_tiles, tiles_per_split, splits;
+  uint4* part_o;    // [group][split][256 rows][128] bf16 (O / l), rows as staged (swizzled 16-byte pieces)
+  float* part_lse;  // [group][split][256]
+  int* arrived;     // [group] splits that have published their partial (zeroed before launch)
   float scale_log2;
   int causal;
+  int q_tma;  // Q tiles by TMA (the stacked rows of 128 / group positions form one box)
   int* status;
 };
 
@@ -110,14 +124,27 @@ __device__ __forceinline__ uint32_t pack2(float a, float b) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
+// Byte offset of 16-byte piece p (0..15, eight bf16) of staged O row `row`:
+// rows of 256 B, pieces XOR-swizzled within each 128-byte half so that a warp
+// writing 32 consecutive rows hits every bank equally.
+__device__ __forceinline__ uint32_t stage_off(int row, int p) {
+  return (uint32_t)row * kStageRow + (uint32_t)(p & 8) * 16u + ((uint32_t)((p & 7) ^ (row & 7)) << 4);
+}
+
+__device__ __forceinline__ float2 unpack2(uint32_t u) {
+  return make_float2(__uint_as_float(u << 16), __uint_as_float(u & 0xFFFF0000u));
+}
+
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_tc(const __grid_constant__ CUtensorMap tk_c, const __grid_constant__ CUtensorMap tv_c,
-                const __grid_constant__ CUtensorMap tk_n, const __grid_constant__ CUtensorMap tv_n, const TcArgs a) {
+                const __grid_constant__ CUtensorMap tk_n, const __grid_constant__ CUtensorMap tv_n,
+                const __grid_constant__ CUtensorMap tq, const TcArgs a) {
   extern __shared__ __align__(1024) uint8_t smem_dyn[];
-  __shared__ __align__(8) uint64_t ring_full[kRing], ring_empty[kRing], s_full[2], s_free[2], p_full[2], p_free[2],
-      drain;
+  __shared__ __align__(8) uint64_t ring_full[kRing], ring_empty[kRing], s_full[2], p_full[2], o_full[2], q_full, drain;
   __shared__ uint32_t tmem_slot;
   __shared__ int abort_flag;
+  __shared__ float s_lse[kBM];                  // per-row lse of this CTA's partial (natural log)
+  __shared__ int s_go;                          // every split of the group has published
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   uint8_t* sm = (uint8_t*)(((uintptr_t)smem_dyn + 1023) & ~(uintptr_t)1023);
@@ -137,22 +164,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   const int n = T1 > T0 ? T1 - T0 : 0;
 
-  // Ring items in load order K0, K1, V0, K2, V1, ..., K(n-1), V(n-2), V(n-1): keys run
-  // one tile ahead of values, so the slot a key tile needs frees a whole tile early.
-  // Item index of K(j): 0 for j = 0, else 2j - 1. Item index of V(j): 2j + 2, or
-  // 2n - 1 for the last tile.
-  auto item_tile = [&](int it, bool& is_v) -> int {
-    if (it == 0) { is_v = false; return 0; }
-    if (it == 2 * n - 1) { is_v = true; return n - 1; }
-    if (it & 1) { is_v = false; return (it + 1) >> 1; }
-    is_v = true;
-    return (it >> 1) - 1;
-  };
-  auto k_item = [&](int jj) { return jj == 0 ? 0 : 2 * jj - 1; };
-  auto v_item = [&](int jj) { return jj == n - 1 ? 2 * n - 1 : 2 * jj + 2; };
+  // ring item it: tile it / 2, K for even it, V for odd it
   auto issue_item = [&](int it) {
-    bool is_v;
-    const int jj = item_tile(it, is_v), t = T0 + jj;
+    const bool is_v = it & 1;
+    const int t = T0 + (it >> 1);
     const int slot = it % kRing;
     const bool cache = t < a.n_cache_tiles;
     const int y = cache ? t * kBN : (t - a.n_cache_tiles) * kBN;
@@ -171,21 +186,31 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int q = 0; q < 2; ++q) {
       mbar_init(smem_addr(&s_full[q]), 1);
-      mbar_init(smem_addr(&s_free[q]), 128);
       mbar_init(smem_addr(&p_full[q]), 128);
-      mbar_init(smem_addr(&p_free[q]), 1);
+      mbar_init(smem_addr(&o_full[q]), 1);
     }
+    mbar_init(smem_addr(&q_full), 1);
     mbar_init(smem_addr(&drain), 1);
     fence_mbar_init();
-    // start the first K/V loads now, so they overlap the Q staging below
+    if (a.q_tma && n > 0) {
+      // Q tile qt = stacked rows [mblk*256 + qt*128, +128) = positions
+      // [that / group, + 128 / group) x every head of the group: one box per 64 columns
+      mbar_expect_tx(smem_addr(&q_full), 2 * kTile);
+      for (int qt = 0; qt < 2; ++qt) {
+        const int i0 = (mblk * kBM + qt * 128) / a.grp;
+        for (int hf = 0; hf < 2; ++hf)
+          tma_load_4d(sbase + kOffQ + qt * kTile + hf * kChunk, &tq, hf * 64, 0, g, i0, smem_addr(&q_full));
+      }
+    }
+    // start the first K/V loads now, so they overlap the set-up below
     for (int it = 0; it < n_pre; ++it) issue_item(it);
   }
   if (warp == 1) {
     tmem_alloc(smem_addr(&tmem_slot), 512);
     tmem_relinquish();
   }
-  // both Q tiles -> shared memory in the swizzled K-major layout (all threads)
-  for (int idx = tid; idx < kBM * 16; idx += kThreads) {
+  // without the Q tensor map: both Q tiles -> shared memory in the swizzled K-major layout (all threads)
+  for (int idx = tid; !a.q_tma && idx < kBM * 16; idx += kThreads) {
     const int r = idx >> 4, ch = idx & 15;
     const int64_t R = (int64_t)mblk * kBM + r;
     const bool ok = R < M;
@@ -205,10 +230,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = tmem_slot;
 
   if (warp == 0) {
-    // ------------------------------------------------ TMA producer: K0 K1 V0 K2 V1 ... through a 3-slot ring
+    // ------------------------------------------------ TMA producer: K0 V0 K1 V1 ... through a 4-slot ring
     if (lane == 0 && n > 0) {
-      bool issued[kRing] = {false, false, false};
-      uint32_t par[kRing] = {0, 0, 0};
+      bool issued[kRing] = {false, false, false, false};
+      uint32_t par[kRing] = {0, 0, 0, 0};
       for (int it = 0; it < n_pre; ++it) issued[it] = true;  // phase 0, issued during set-up
       for (int it = n_pre; it < 2 * n; ++it) {
         const int slot = it % kRing;
@@ -224,17 +249,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else if (warp == 1) {
     // ------------------------------------------------ MMA issuer
-    // order: S0(0) S1(0) | S0(1) S1(1) PV0(0) PV1(0) | S0(2) S1(2) PV0(1) PV1(1) | ...
-    // Each group's next S is issued as soon as that group has loaded its current
-    // S, so both softmax groups work on a tile at the same time.
+    // S0(0) S1(0) | PV0(0) S0(1) PV1(0) S1(1) | PV0(1) S0(2) PV1(1) S1(2) | ...
+    // S_q(j+1) overwrites the TMEM columns PV_q(j) reads P from; the tensor
+    // core runs one thread's MMAs in issue order. Each s_full commit also
+    // covers PV_q(j), so the softmax may rescale O_q as soon as S_q(j+1) lands.
     if (lane == 0 && n > 0) {
       const uint32_t id_s = idesc_bf16_f32(128, kBN, 0, 0);
       const uint32_t id_o = idesc_bf16_f32(128, kHD, 0, 1);
-      auto issue_s = [&](int q, int jj) -> bool {
-        const int it = k_item(jj), slot = it % kRing;
-        if (!wait_bar(smem_addr(&ring_full[slot]), (uint32_t)(it / kRing) & 1u, ctl)) return false;
-        if (jj > 0 && !wait_bar(smem_addr(&s_free[q]), (uint32_t)(jj - 1) & 1u, ctl)) return false;
-        tc_fence_after();
+      auto item_ready = [&](int it) -> bool {
+        return wait_bar(smem_addr(&ring_full[it % kRing]), (uint32_t)(it / kRing) & 1u, ctl);
+      };
+      auto mma_s = [&](int q, int slot) {
         const uint32_t kb = sbase + kOffRing + slot * kTile, qb = sbase + kOffQ + q * kTile;
 #pragma unroll
         for (int kk = 0; kk < kHD / 16; ++kk) {
@@ -242,31 +267,49 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint64_t bd = sdesc_sw128(kb + (kk >> 2) * kChunk + (kk & 3) * 32, 0, 1024);
           mma_bf16(tmem + q * 128, ad, bd, id_s, kk > 0);
         }
-        mma_commit(smem_addr(&s_full[q]));
-        if (q == 1) mma_commit(smem_addr(&ring_empty[slot]));  // K(jj) consumed by both tiles
-        return true;
       };
-      auto issue_pv = [&](int q, int jj) -> bool {
-        const int it = v_item(jj), slot = it % kRing;
-        if (!wait_bar(smem_addr(&ring_full[slot]), (uint32_t)(it / kRing) & 1u, ctl)) return false;
-        if (!wait_bar(smem_addr(&p_full[q]), (uint32_t)jj & 1u, ctl)) return false;
-        tc_fence_after();
-        const uint32_t pb = sbase + kOffP + q * kTile, vb = sbase + kOffRing + slot * kTile;
+      auto mma_pv = [&](int q, int slot, bool acc) {
+        const uint32_t vb = sbase + kOffRing + slot * kTile;
 #pragma unroll
         for (int kk = 0; kk < kBN / 16; ++kk) {
-          const uint64_t ad = sdesc_sw128(pb + (kk >> 2) * kChunk + (kk & 3) * 32, 0, 1024);
           const uint64_t bd = sdesc_sw128(vb + kk * 2048, kChunk, 1024);
-          mma_bf16(tmem + 256 + q * 128, ad, bd, id_o, (jj > 0 || kk > 0) ? 1u : 0u);
+          mma_bf16_ts(tmem + 256 + q * 128, tmem + q * 128 + kk * 8, bd, id_o, (acc || kk > 0) ? 1u : 0u);
         }
-        mma_commit(smem_addr(&p_free[q]));
-        if (q == 1) mma_commit(smem_addr(&ring_empty[slot]));  // V(jj) consumed by both tiles
-        return true;
       };
-      bool ok = issue_s(0, 0) && issue_s(1, 0);
+      bool ok = item_ready(0) && (!a.q_tma || wait_bar(smem_addr(&q_full), 0, ctl));
+      if (ok) {
+        mma_s(0, 0);
+        mma_commit(smem_addr(&s_full[0]));
+        mma_s(1, 0);
+        mma_commit(smem_addr(&s_full[1]));
+        mma_commit(smem_addr(&ring_empty[0]));  // K(0) consumed
+      }
       for (int jj = 0; jj < n && ok; ++jj) {
-        if (jj + 1 < n && !(issue_s(0, jj + 1) && issue_s(1, jj + 1))) break;
-        if (!issue_pv(0, jj)) break;
-        if (!issue_pv(1, jj)) break;
+        const int it_v = 2 * jj + 1, it_k = 2 * jj + 2;
+        const int sv = it_v % kRing, sk = it_k % kRing;
+        const bool more = jj + 1 < n;
+        if (!item_ready(it_v)) break;
+        if (!wait_bar(smem_addr(&p_full[0]), (uint32_t)jj & 1u, ctl)) break;
+        tc_fence_after();
+        mma_pv(0, sv, jj > 0);
+        if (more) {
+          if (!item_ready(it_k)) break;
+          mma_s(0, sk);
+          mma_commit(smem_addr(&s_full[0]));
+        } else {
+          mma_commit(smem_addr(&o_full[0]));
+        }
+        if (!wait_bar(smem_addr(&p_full[1]), (uint32_t)jj & 1u, ctl)) break;
+        tc_fence_after();
+        mma_pv(1, sv, jj > 0);
+        mma_commit(smem_addr(&ring_empty[sv]));  // V(jj) consumed
+        if (more) {
+          mma_s(1, sk);
+          mma_commit(smem_addr(&s_full[1]));
+          mma_commit(smem_addr(&ring_empty[sk]));  // K(jj+1) consumed
+        } else {
+          mma_commit(smem_addr(&o_full[1]));
+        }
       }
       mma_commit(smem_addr(&drain));
       wait_bar(smem_addr(&drain), 0, ctl);
@@ -277,12 +320,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int q = (warp - 2) >> 2;
     const int q4 = warp & 3;
     const int r = q4 * 32 + lane;
+    const int rt = q * 128 + r;  // row within the CTA's 256
     const uint32_t loff = (uint32_t)(q4 * 32) << 16;
     const uint32_t tS = tmem + q * 128, tO = tmem + 256 + q * 128;
-    const int64_t R = (int64_t)mblk * kBM + q * 128 + r;
+    const int64_t R = (int64_t)mblk * kBM + rt;
     const bool row_ok = R < M;
     const int64_t i = row_ok ? R / a.grp : 0;
-    const int64_t h = (int64_t)g * a.grp + (row_ok ? R % a.grp : 0);
     float ref = -INFINITY, l = 0.f;
     bool ok = true;
     int done_tiles = 0;
@@ -300,23 +343,26 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool got = wait_bar(smem_addr(&s_full[q]), (uint32_t)jj & 1u, ctl);
       if (grp_any(q, !got)) { ok = false; break; }
       tc_fence_after();
-      float v[kBN];
-      tmem_ld128(tS + loff, v);  // the whole S row of this tile, one load, one wait
-      tc_fence_before();
-      mbar_arrive(smem_addr(&s_free[q]));  // the MMA may overwrite S now
-      if (lim < kBN) {
+      // Two reads of the S row: the whole row for its max (one 128-column
+      // load), then 32-column chunks for P = exp2(s - ref), packed bf16x2 in
+      // registers until the row is done.
+      float mx;
+      {
+        float v[kBN];
+        tmem_ld128(tS + loff, v);
+        if (lim < kBN) {
 #pragma unroll
-        for (int e = 0; e < kBN; ++e)
-          if (e >= lim) v[e] = -INFINITY;
+          for (int e = 0; e < kBN; ++e)
+            if (e >= lim) v[e] = -INFINITY;
+        }
+        float m8[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) m8[e] = v[e];
+#pragma unroll
+        for (int e = 8; e < kBN; ++e) m8[e & 7] = fmaxf(m8[e & 7], v[e]);
+        mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])), fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
       }
-      float mx8[8];
-#pragma unroll
-      for (int e = 0; e < 8; ++e) mx8[e] = v[e];
-#pragma unroll
-      for (int e = 8; e < kBN; ++e) mx8[e & 7] = fmaxf(mx8[e & 7], v[e]);
-      float mt = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                       fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
-      mt *= a.scale_log2;  // scale > 0 keeps the order
+      const float mt = mx * a.scale_log2;  // scale > 0 keeps the order
       bool need = false;
       float factor = 1.f;
       if (mt > -INFINITY) {
@@ -329,39 +375,38 @@ __global__ void __launch_bounds__(kThreads, 1)
           l *= factor;
         }
       }
-      // P row of this tile, packed to bf16 in registers while PV(jj-1) may still run
       const float rr = ref == -INFINITY ? 0.f : ref;
+      uint32_t pk[kBN / 2];
       float sum8[8];
 #pragma unroll
       for (int e = 0; e < 8; ++e) sum8[e] = 0.f;
-      uint32_t pk[kBN / 2];
 #pragma unroll
-      for (int c = 0; c < kBN / 8; ++c) {
-        float p8[8];
+      for (int c = 0; c < 4; ++c) {
+        float s32[32];
+        tmem_ld32(tS + loff + c * 32, s32);
+        if (lim < (c + 1) * 32) {
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          p8[e] = ex2_approx(fmaf(v[c * 8 + e], a.scale_log2, -rr));  // exp2(-inf) = 0 for masked keys
-          sum8[e] += p8[e];
+          for (int e = 0; e < 32; ++e)
+            if (c * 32 + e >= lim) s32[e] = -INFINITY;
         }
 #pragma unroll
-        for (int e = 0; e < 4; ++e) pk[c * 4 + e] = pack2(p8[2 * e], p8[2 * e + 1]);
-      }
-      // PV(jj-1) must be complete both before P is overwritten and before O is rescaled
-      if (jj > 0) {
-        const bool pf = wait_bar(smem_addr(&p_free[q]), (uint32_t)(jj - 1) & 1u, ctl);
-        if (grp_any(q, !pf)) { ok = false; break; }
-        tc_fence_after();
-      }
-      uint8_t* prow = sm + kOffP + q * kTile + r * 128;
+        for (int g8 = 0; g8 < 4; ++g8) {
+          float p8[8];
 #pragma unroll
-      for (int c = 0; c < kBN / 8; ++c) {
-        const int chunk = c >> 3, piece = c & 7;
-        *reinterpret_cast<uint4*>(prow + chunk * kChunk + ((piece ^ (r & 7)) << 4)) =
-            make_uint4(pk[c * 4], pk[c * 4 + 1], pk[c * 4 + 2], pk[c * 4 + 3]);
+          for (int e = 0; e < 8; ++e) {
+            p8[e] = ex2_approx(fmaf(s32[g8 * 8 + e], a.scale_log2, -rr));  // exp2(-inf) = 0 when masked
+            sum8[e] += p8[e];
+          }
+#pragma unroll
+          for (int e = 0; e < 4; ++e) pk[c * 16 + g8 * 4 + e] = pack2(p8[2 * e], p8[2 * e + 1]);
+        }
       }
+      // P over the first 64 columns of S_q (S is no longer needed)
+      tmem_st32_async(tS + loff, pk);
+      tmem_st32_async(tS + loff + 32, pk + 32);
       l += ((sum8[0] + sum8[1]) + (sum8[2] + sum8[3])) + ((sum8[4] + sum8[5]) + (sum8[6] + sum8[7]));
-      // O holds every PV issued so far (waited above); rescale it before PV(jj) adds to it.
-      // Done after P is formed so the S row and the O chunk are never live together.
+      // O_q holds every PV_q issued so far (complete: covered by this tile's
+      // s_full commit); rescale it before PV_q(jj) adds to it.
       if (__any_sync(0xffffffffu, need)) {
 #pragma unroll 1
         for (int c = 0; c < 4; ++c) {
@@ -372,55 +417,145 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_st32(tO + loff + c * 32, o);
         }
       }
+      tmem_wait_st();
       tc_fence_before();
-      fence_proxy_async_smem();
       mbar_arrive(smem_addr(&p_full[q]));
       done_tiles = jj + 1;
     }
-    // epilogue
+    // epilogue: stage O_q / l (bf16) and the row's lse for the split merge.
+    // The staged rows (64 KB) overwrite the Q tiles: every S product is
+    // complete once o_full[0] fires.
     bool have = ok && done_tiles == n && n > 0;
     if (have) {
-      const bool od = wait_bar(smem_addr(&p_free[q]), (uint32_t)(n - 1) & 1u, ctl);
+      const bool od = wait_bar(smem_addr(&o_full[q]), 0, ctl);
       have = !grp_any(q, !od);
       tc_fence_after();
     }
     const float inv = l > 0.f ? 1.f / l : 0.f;
-    const float lse_v = l > 0.f ? (ref + log2f(l)) * kLn2 : -INFINITY;
+    const float lse_v = (have && l > 0.f) ? (ref + log2f(l)) * kLn2 : -INFINITY;
 #pragma unroll
     for (int c = 0; c < 4; ++c) {
-      float v[32];
+      float o[32];
       if (have) {
-        tmem_ld32(tO + loff + c * 32, v);
+        tmem_ld32(tO + loff + c * 32, o);
       } else {
 #pragma unroll
-        for (int e = 0; e < 32; ++e) v[e] = 0.f;
+        for (int e = 0; e < 32; ++e) o[e] = 0.f;
       }
-      if (!row_ok) continue;
-      if (a.splits == 1) {
-        __nv_bfloat16* dst = a.out + (i * a.Hq + h) * kHD + c * 32;
 #pragma unroll
-        for (int e = 0; e < 32; e += 8) {
-          uint4 w = make_uint4(pack2(v[e] * inv, v[e + 1] * inv), pack2(v[e + 2] * inv, v[e + 3] * inv),
-                               pack2(v[e + 4] * inv, v[e + 5] * inv), pack2(v[e + 6] * inv, v[e + 7] * inv));
-          *reinterpret_cast<uint4*>(dst + e) = w;
-        }
-      } else {
-        float* dst = a.part_o + (((int64_t)split * a.C + i) * a.Hq + h) * kHD + c * 32;
-#pragma unroll
-        for (int e = 0; e < 32; e += 4)
-          *reinterpret_cast<float4*>(dst + e) = make_float4(v[e] * inv, v[e + 1] * inv, v[e + 2] * inv, v[e + 3] * inv);
-      }
+      for (int e = 0; e < 4; ++e)
+        *reinterpret_cast<uint4*>(sm + stage_off(rt, c * 4 + e)) =
+            make_uint4(pack2(o[e * 8] * inv, o[e * 8 + 1] * inv), pack2(o[e * 8 + 2] * inv, o[e * 8 + 3] * inv),
+                       pack2(o[e * 8 + 4] * inv, o[e * 8 + 5] * inv), pack2(o[e * 8 + 6] * inv, o[e * 8 + 7] * inv));
     }
-    if (row_ok) {
-      if (a.splits == 1) {
-        if (a.lse) a.lse[h * a.C + i] = lse_v;
-      } else {
-        a.part_lse[((int64_t)split * a.Hq + h) * a.C + i] = lse_v;
-      }
-    }
+    s_lse[rt] = row_ok ? lse_v : -INFINITY;
   }
+  fence_proxy_async_smem();  // staged rows -> the bulk copy below
   tc_fence_before();
   __syncthreads();
+
+  // ------------------------------------------------ publish this split's partial, then merge
+  const int grp_id = g * gridDim.x + mblk;
+  const int cs = a.splits;
+  constexpr int kRowPieces = kHD / 8;  // 16-byte pieces of a staged row
+  {
+    if (tid == 0) {
+      bulk_store(a.part_o + ((size_t)grp_id * cs + split) * (kBM * kRowPieces), sbase, kBM * kStageRow);
+      bulk_commit();
+    }
+    float* pl = a.part_lse + ((size_t)grp_id * cs + split) * kBM;
+    for (int x = tid; x < kBM; x += kThreads) pl[x] = s_lse[x];
+    __threadfence();
+    __syncthreads();
+    if (tid == 0) {
+      bulk_wait_all();
+      fence_proxy_async_global();  // the bulk-copied rows, before the release below
+      red_release_add_gpu(a.arrived + grp_id, 1);
+      bool go = true;
+      const long long t0 = clock64();
+      while ((int)ld_acquire_gpu(a.arrived + grp_id) < cs) {
+        if (abort_flag || clock64() - t0 > kTimeoutCycles) {
+          latch(a.status, DG_ERR_TIMEOUT);
+          go = false;
+          break;
+        }
+        __nanosleep(32);
+      }
+      s_go = go;
+    }
+    __syncthreads();
+  }
+  if (s_go) {
+    // Rows [r0, r0 + nr) of the group are merged by this CTA, two 16-byte
+    // pieces (16 columns) per item, so that one round of loads usually covers
+    // a thread's work: the item's lse values and pieces of up to 12 splits
+    // are loaded at once, then combined with weights exp(lse_s - max) (an
+    // online rescale joins further batches of 12 splits).
+    constexpr int kBatch = 12;
+    constexpr int kItemsPerRow = kRowPieces / 2;
+    const int rpc = (kBM + cs - 1) / cs;
+    const int r0 = split * rpc;
+    const int nr = max(0, min(kBM, r0 + rpc) - r0);
+    const float* pl = a.part_lse + (size_t)grp_id * cs * kBM;
+    const uint4* pg = a.part_o + (size_t)grp_id * cs * (kBM * kRowPieces);
+    for (int item = tid; item < nr * kItemsPerRow; item += kThreads) {
+      const int t = item / kItemsPerRow, pc = (item % kItemsPerRow) * 2;
+      const int row = r0 + t;
+      const int64_t R = (int64_t)mblk * kBM + row;
+      if (R >= M) continue;
+      const uint4* src0 = pg + stage_off(row, pc) / 16;
+      const uint4* src1 = pg + stage_off(row, pc + 1) / 16;
+      float acc[16];
+#pragma unroll
+      for (int e = 0; e < 16; ++e) acc[e] = 0.f;
+      float m = -INFINITY, tot = 0.f;
+      for (int s0 = 0; s0 < cs; s0 += kBatch) {
+        float lv[kBatch];
+        uint4 x0[kBatch], x1[kBatch];
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u) {
+          lv[u] = -INFINITY;
+          if (s0 + u < cs) {
+            const size_t so = (size_t)(s0 + u) * (kBM * kRowPieces);
+            lv[u] = __ldcg(pl + (size_t)(s0 + u) * kBM + row);
+            x0[u] = __ldcg(src0 + so);
+            x1[u] = __ldcg(src1 + so);
+          }
+        }
+        float bm = m;
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u) bm = fmaxf(bm, lv[u]);
+        if (bm == -INFINITY) continue;
+        const float f = __expf(m - bm);  // 0 while m = -inf
+        tot *= f;
+#pragma unroll
+        for (int e = 0; e < 16; ++e) acc[e] *= f;
+        m = bm;
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u) {
+          if (s0 + u < cs && lv[u] > -INFINITY) {
+            const float w = __expf(lv[u] - m);
+            tot += w;
+            const uint32_t wd[8] = {x0[u].x, x0[u].y, x0[u].z, x0[u].w, x1[u].x, x1[u].y, x1[u].z, x1[u].w};
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+              const float2 fv = unpack2(wd[e]);
+              acc[2 * e] = fmaf(w, fv.x, acc[2 * e]);
+              acc[2 * e + 1] = fmaf(w, fv.y, acc[2 * e + 1]);
+            }
+          }
+        }
+      }
+      const float it = tot > 0.f ? 1.f / tot : 0.f;
+      const int64_t i = R / a.grp, h = (int64_t)g * a.grp + R % a.grp;
+      uint4* dst = reinterpret_cast<uint4*>(a.out + (i * a.Hq + h) * kHD + pc * 8);
+      dst[0] = make_uint4(pack2(acc[0] * it, acc[1] * it), pack2(acc[2] * it, acc[3] * it),
+                          pack2(acc[4] * it, acc[5] * it), pack2(acc[6] * it, acc[7] * it));
+      dst[1] = make_uint4(pack2(acc[8] * it, acc[9] * it), pack2(acc[10] * it, acc[11] * it),
+                          pack2(acc[12] * it, acc[13] * it), pack2(acc[14] * it, acc[15] * it));
+      if (pc == 0 && a.lse) a.lse[h * a.C + i] = tot > 0.f ? m + logf(tot) : -INFINITY;
+    }
+  }
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);
@@ -436,6 +571,17 @@ bool make_kv_map(CUtensorMap* m, const void* base, int64_t rows, int64_t rows_al
   return tmap_bf16_sw128(m, base, 3, dims, strides, box);
 }
 
+// q [C][Hq][128] bf16 viewed as [C][Hkv][group][128]: box [128 / group positions]
+// [1 KV head][group heads][64 columns], so one box is 128 stacked rows
+// (position-major, head-in-group minor) of one KV head's queries.
+bool make_q_map(CUtensorMap* m, const void* q, int C, int Hq, int Hkv) {
+  const int grp = Hq / Hkv;
+  const uint64_t dims[4] = {(uint64_t)kHD, (uint64_t)grp, (uint64_t)Hkv, (uint64_t)C};
+  const uint64_t strides[3] = {(uint64_t)kHD * 2, (uint64_t)grp * kHD * 2, (uint64_t)Hq * kHD * 2};
+  const uint32_t box[4] = {64, (uint32_t)grp, 1, (uint32_t)(128 / grp)};
+  return tmap_bf16_sw128(m, q, 4, dims, strides, box);
+}
+
 int num_sms() {
   static int n = 0;
   if (!n) {
@@ -449,9 +595,20 @@ int num_sms() {
   return n;
 }
 
+// Kernel attribute (dynamic shared memory), set once.
+cudaError_t prepare_kernel() {
+  static std::once_flag once;
+  static cudaError_t err = cudaSuccess;
+  std::call_once(once, [] {
+    err = cudaFuncSetAttribute(attn_fwd_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmem + 1024);
+  });
+  return err;
+}
+
 }  // namespace
 
-// Split plan of the tensor-core path: one wave of CTAs (one per SM).
+// Split plan of the tensor-core path: one wave of CTAs, one per SM (the
+// launch is cooperative, so the grid must fit on the GPU at once).
 void attn_tc_plan(int C, int Hq, int Hkv, int64_t P, int* splits, int* tiles_per_split) {
   const int64_t M = (int64_t)(Hq / Hkv) * C;
   const int64_t base = ((M + kBM - 1) / kBM) * Hkv;
@@ -462,20 +619,49 @@ void attn_tc_plan(int C, int Hq, int Hkv, int64_t P, int* splits, int* tiles_per
     const int x = v ? atoi(v) : 0;
     return x > 0 ? x : 0;
   }();
-  int want = env_splits ? env_splits : (int)(num_sms() / base);
-  if (want < 1) want = 1;
+  int want = (int)(num_sms() / base);
+  if (env_splits && env_splits < want) want = env_splits;
   if (want > tiles) want = tiles;
-  if (want > 64) want = 64;
+  if (want > kMaxSplits) want = kMaxSplits;
+  if (want < 1) want = 1;
   const int tps = (tiles + want - 1) / want;
   if (tiles_per_split) *tiles_per_split = tps;
   *splits = (tiles + tps - 1) / tps;
 }
 
+// Workspace: per (row block, KV head) group and split, the staged bf16 O rows
+// and the row lse; then one arrival counter per group.
+struct TcLayout {
+  size_t part_o, part_lse, arrived, total;
+  int64_t groups;
+};
+TcLayout tc_layout(int C, int Hq, int Hkv, int64_t P) {
+  int splits = 1;
+  attn_tc_plan(C, Hq, Hkv, P, &splits, nullptr);
+  TcLayout L;
+  const int64_t M = (int64_t)(Hq / Hkv) * C;
+  L.groups = ((M + kBM - 1) / kBM) * Hkv;
+  auto al = [](size_t x) { return (x + 255) & ~(size_t)255; };
+  L.part_o = 0;
+  L.part_lse = al((size_t)L.groups * splits * kBM * kHD * sizeof(__nv_bfloat16));
+  L.arrived = L.part_lse + al((size_t)L.groups * splits * kBM * sizeof(float));
+  L.total = L.arrived + al((size_t)L.groups * sizeof(int));
+  return L;
+}
+
+size_t attn_tc_workspace(int C, int Hq, int Hkv, int64_t P) {
+  if (C < 1 || Hkv < 1 || Hq % Hkv) return 0;
+  return tc_layout(C, Hq, Hkv, P).total;
+}
+
 int attn_tc_launch(const void* q, const void* k_cache, const void* v_cache, int64_t cap, int64_t P,
                    const void* k_canvas, const void* v_canvas, void* out, float* lse, int C, int Hq, int Hkv,
                    float scale, int mask, void* ws, size_t ws_bytes, cudaStream_t s) {
+  DG_CUDA_TRY(prepare_kernel());
   int splits, tps;
   attn_tc_plan(C, Hq, Hkv, P, &splits, &tps);
+  const TcLayout L = tc_layout(C, Hq, Hkv, P);
+  if (!ws || ws_bytes < L.total || ((uintptr_t)ws & 255u)) return DG_ERR_WORKSPACE;
   int* st = status_ptr();
   if (!st) return DG_ERR_CUDA;
   CUtensorMap tk_c, tv_c, tk_n, tv_n;
@@ -484,6 +670,10 @@ int attn_tc_launch(const void* q, const void* k_cache, const void* v_cache, int6
   if (P > 0 && (!make_kv_map(&tk_c, k_cache, P, cap, Hkv) || !make_kv_map(&tv_c, v_cache, P, cap, Hkv)))
     return DG_ERR_CUDA;
   if (!make_kv_map(&tk_n, k_canvas, C, C, Hkv) || !make_kv_map(&tv_n, v_canvas, C, C, Hkv)) return DG_ERR_CUDA;
+  const int grp = Hq / Hkv;
+  CUtensorMap tq;
+  memset(&tq, 0, sizeof(tq));
+  const bool q_tma = 128 % grp == 0 && make_q_map(&tq, q, C, Hq, Hkv);
   TcArgs a;
   a.q = (const __nv_bfloat16*)q;
   a.out = (__nv_bfloat16*)out;
@@ -497,29 +687,26 @@ int attn_tc_launch(const void* q, const void* k_cache, const void* v_cache, int6
   a.n_tiles = a.n_cache_tiles + (C + kBN - 1) / kBN;
   a.tiles_per_split = tps;
   a.splits = splits;
+  a.part_o = (uint4*)((char*)ws + L.part_o);
+  a.part_lse = (float*)((char*)ws + L.part_lse);
+  a.arrived = (int*)((char*)ws + L.arrived);
   a.scale_log2 = scale * 1.4426950408889634f;
   a.causal = mask == DG_MASK_CAUSAL_BLOCK;
+  a.q_tma = q_tma;
   a.status = st;
-  a.part_o = nullptr;
-  a.part_lse = nullptr;
-  if (splits > 1) {
-    size_t o = (size_t)splits * C * Hq * kHD * sizeof(float);
-    o = (o + 255) & ~(size_t)255;
-    if (ws_bytes < o + (size_t)splits * Hq * C * sizeof(float)) return DG_ERR_WORKSPACE;
-    a.part_o = (float*)ws;
-    a.part_lse = (float*)((char*)ws + o);
-  }
-  static std::once_flag once;
-  static cudaError_t attr_err = cudaSuccess;
-  std::call_once(once, [] {
-    attr_err = cudaFuncSetAttribute(attn_fwd_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmem + 1024);
-  });
-  DG_CUDA_TRY(attr_err);
   const int64_t M = (int64_t)a.grp * C;
-  dim3 grid((unsigned)((M + kBM - 1) / kBM), Hkv, splits);
-  attn_fwd_tc<<<grid, kThreads, kSmem + 1024, s>>>(tk_c, tv_c, tk_n, tv_n, a);
-  DG_LAUNCH_CHECK();
-  if (splits > 1) return attn_combine_launch(a.part_o, a.part_lse, a.out, lse, C, Hq, kHD, splits, s);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)((M + kBM - 1) / kBM), Hkv, splits);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = kSmem + 1024;
+  cfg.stream = s;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeCooperative;
+  at[0].val.cooperative = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  DG_CUDA_TRY(cudaMemsetAsync(a.arrived, 0, (size_t)L.groups * sizeof(int), s));
+  DG_CUDA_TRY(cudaLaunchKernelEx(&cfg, attn_fwd_tc, tk_c, tv_c, tk_n, tv_n, tq, a));
   return DG_OK;
 }
 

@@ -18,10 +18,16 @@ __device__ __forceinline__ void latch(int* status, int code) {
 
 int* status_ptr();  // device address of the status word for the current device (api.cu)
 
-#define DG_CUDA_TRY(expr)                       \
-  do {                                          \
-    cudaError_t e_ = (expr);                    \
-    if (e_ != cudaSuccess) return DG_ERR_CUDA;  \
+// Reports a failed CUDA call on stderr when DG_VERBOSE is set (defined in api.cu).
+void report_cuda_error(cudaError_t e, const char* what, const char* file, int line);
+
+#define DG_CUDA_TRY(expr)                                          \
+  do {                                                             \
+    cudaError_t e_ = (expr);                                       \
+    if (e_ != cudaSuccess) {                                       \
+      ::dg::report_cuda_error(e_, #expr, __FILE__, __LINE__);      \
+      return DG_ERR_CUDA;                                          \
+    }                                                              \
   } while (0)
 
 #define DG_LAUNCH_CHECK() DG_CUDA_TRY(cudaGetLastError())
@@ -74,6 +80,7 @@ void attn_tc_plan(int C, int Hq, int Hkv, int64_t P, int* splits, int* tiles_per
 int attn_tc_launch(const void* q, const void* k_cache, const void* v_cache, int64_t cap, int64_t P,
                    const void* k_canvas, const void* v_canvas, void* out, float* lse, int C, int Hq, int Hkv,
                    float scale, int mask, void* ws, size_t ws_bytes, cudaStream_t s);
+size_t attn_tc_workspace(int C, int Hq, int Hkv, int64_t P);
 
 int vocab_simt_launch(const float* h, const float* emb, int C, int V, int d, int32_t* argmax, float* conf,
                       float* lse, float* selfcond, cudaStream_t s);

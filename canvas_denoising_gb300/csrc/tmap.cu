@@ -31,8 +31,8 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 struct Key {
   const void* base;
   int rank;
-  uint64_t dims[3], strides[2];
-  uint32_t box[3];
+  uint64_t dims[5], strides[4];
+  uint32_t box[5];
   bool operator==(const Key& o) const { return memcmp(this, &o, sizeof(Key)) == 0; }
 };
 
@@ -51,7 +51,7 @@ int g_next = 0;
 
 bool tmap_bf16_sw128(CUtensorMap* out, const void* base, int rank, const uint64_t* dims, const uint64_t* strides,
                      const uint32_t* box) {
-  if (rank < 2 || rank > 3) return false;
+  if (rank < 2 || rank > 5) return false;
   Key k;
   memset(&k, 0, sizeof(k));
   k.base = base;
@@ -71,8 +71,8 @@ bool tmap_bf16_sw128(CUtensorMap* out, const void* base, int rank, const uint64_
   }
   auto fn = encode_fn();
   if (!fn) return false;
-  cuuint64_t d[3], s[2];
-  cuuint32_t b[3], e[3] = {1, 1, 1};
+  cuuint64_t d[5], s[4];
+  cuuint32_t b[5], e[5] = {1, 1, 1, 1, 1};
   for (int i = 0; i < rank; ++i) {
     d[i] = dims[i];
     b[i] = box[i];
