@@ -198,10 +198,14 @@ class Canvas:
         if j == 0:
             B.canvas_init(self.tokens, w.V, self.seed, self.P, stream=stream)
             n += 1
+        if ev is not None:
+            ev[2].record(stream)
         B.canvas_attn(q, self.k, self.v, self.P, kn, vn, out=self.out, lse=self.lse_attn, workspace=self.ws_attn,
                       stream=stream)
-        n += 2 if self.ws_attn.numel() > 256 else 1
+        # head_dim 128: one kernel (key splits merged in-kernel); otherwise + a combine when split
+        n += 1 if w.hd == 128 else (2 if self.ws_attn.numel() > 256 else 1)
         if ev is not None:
+            ev[3].record(stream)
             ev[0].record(stream)
         # vocabulary step with the threshold re-noise fused into its last kernel
         B.vocab_step_renoise(h, self.emb, self.tokens, w.thresholds[0], self.seed, j, self.P, argmax=self.argmax,
@@ -254,7 +258,7 @@ def run_ours(args, world, rank, local):
     launches = 0
     replays = K // spc if graph is not None else 0
     eager = K - replays * spc
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(eager)]
+    evs = [tuple(torch.cuda.Event(enable_timing=True) for _ in range(4)) for _ in range(eager)]
     with torch.cuda.stream(stream):
         t0.record(stream)
         for _ in range(replays):
@@ -272,7 +276,8 @@ def run_ours(args, world, rank, local):
         torch.distributed.barrier()
     ms = t0.elapsed_time(t1)
     status = B.device_status(stream)
-    vocab_ms = statistics.mean(a.elapsed_time(b) for a, b in evs)
+    vocab_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
+    attn_ms = statistics.mean(e[2].elapsed_time(e[3]) for e in evs)
     ms = max_over_ranks(ms, dev)
 
     # ---- end to end through the public API: per-step inputs from pinned host memory, result back
@@ -317,6 +322,14 @@ def run_ours(args, world, rank, local):
             "frac": round(achieved / pk["bf16_tflops"], 4), "traffic": traffic,
             "peak_source": f"{pk['source']} bf16 burst", "algorithmic_flops_per_launch": flops,
             "avg_launch_ms": round(vocab_ms, 4)}
+    # the step's other contraction: canvas attention (one launch; timed the same way)
+    aflops = 4.0 * w.C * (w.prefix + w.C) * w.hd * w.Hq
+    a_ach = aflops / (attn_ms / 1e3) / 1e12
+    roof_attn = {"kernel": "dg_canvas_attn (attn_fwd_tc)", "bound": "tensor", "achieved": round(a_ach, 1),
+                 "peak": pk["bf16_tflops"], "unit": "TFLOP/s", "frac": round(a_ach / pk["bf16_tflops"], 4),
+                 "traffic": committed_traffic("attn_fwd_tc", args.workload),
+                 "peak_source": f"{pk['source']} bf16 burst", "algorithmic_flops_per_launch": aflops,
+                 "avg_launch_ms": round(attn_ms, 4)}
     steps_per_s = job_rate(world, K, ms)
     line = {
         "metric": metric_name(), "value": round(steps_per_s, 3), "unit": "steps/s", "n_gpus": world, "steps": K,
@@ -328,6 +341,7 @@ def run_ours(args, world, rank, local):
                    "steps_per_canvas": w.steps, "alpha": w.alpha, "parallelism": f"replicas{world}",
                    "l2": "inputs larger than L2 (embedding table %.2f GB), no flush" % (w.V * w.d * 2 / 1e9)},
         "roofline": roof,
+        "roofline_attention": roof_attn,
         "gpu_launches": launches * world,
         "cuda_graph": bool(replays), 
         "clocks": clk, "device_status": status,
@@ -343,12 +357,12 @@ def run_ours(args, world, rank, local):
 
 def capture_canvas_graph(cv, stream, spc):
     """Captures one canvas (init, spc denoising steps, append) as a CUDA graph,
-    with timing events around each vocabulary step as event nodes. Returns
+    with timing events around each step's attention and vocabulary calls as
+    event nodes. Returns
     (graph, events, kernel launches per replay), or (None, None, 0) if this
     torch cannot record timing events inside a graph."""
     try:
-        evs = [(torch.cuda.Event(enable_timing=True, external=True),
-                torch.cuda.Event(enable_timing=True, external=True)) for _ in range(spc)]
+        evs = [tuple(torch.cuda.Event(enable_timing=True, external=True) for _ in range(4)) for _ in range(spc)]
     except TypeError:
         return None, None, 0
     g = torch.cuda.CUDAGraph()
