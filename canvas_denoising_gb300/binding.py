@@ -43,6 +43,11 @@ _SIGS = {
     "dg_canvas_init": (_c_int, [_p, _c_int, _c_int, _c_u64, _c_i64, _p]),
     "dg_kv_append": (_c_int, [_p, _p, _c_i64, ctypes.POINTER(_c_i64), _p, _p, _c_int, _c_int, _c_int, _c_int, _p,
                               _c_int, _p, _p, _p, _c_sz, _p]),
+    "dg_selfcond_input": (_c_int, [_p, _p, _p, _p, _c_int, _c_int, _c_int, _c_int, _p]),
+    "dg_token_prob": (_c_int, [_p, _p, _p, _p, _p, _c_int, _c_int, _c_int, _c_int, _p]),
+    "dg_unmask": (_c_int, [_p, _p, _p, _c_int, ctypes.c_int32, _c_f, _p, _p]),
+    "dg_canvas_fill": (_c_int, [_p, _c_int, ctypes.c_int32, _p]),
+    "dg_count_flags": (_c_int, [_p, _c_int, _p, _p]),
 }
 
 EXPORTS = tuple(_SIGS)
@@ -267,3 +272,58 @@ def kv_append(k_cache, v_cache, length: int, k_new, v_new, q_new=None, out=None,
                              dt, _ptr(q_new), Hq, _ptr(out), _ptr(lse), _ptr(workspace), ws_bytes, _stream(stream))
     _check("dg_kv_append", rc)
     return n.value, out, lse
+
+
+# ------------------------------------------------------------------ next to the step
+def selfcond_input(tokens, emb, selfcond=None, x=None, stream=None):
+    """x[i] = emb[tokens[i]] + selfcond[i] (the next step's stand-in input)."""
+    for t, n in ((tokens, "tokens"), (emb, "emb"), (selfcond, "selfcond"), (x, "x")):
+        _need(t, n)
+    C = tokens.shape[0]
+    V, d = emb.shape
+    if x is None:
+        x = torch.empty((C, d), dtype=emb.dtype, device=emb.device)
+    rc = load().dg_selfcond_input(_ptr(tokens), _ptr(emb), _ptr(selfcond), _ptr(x), C, V, d, _dtype_code(emb),
+                                  _stream(stream))
+    _check("dg_selfcond_input", rc)
+    return x
+
+
+def token_prob(h, emb, tokens, lse, prob=None, stream=None):
+    """prob[i] = exp(h[i] . emb[tokens[i]] - lse[i]): the current token's probability."""
+    for t, n in ((h, "h"), (emb, "emb"), (tokens, "tokens"), (lse, "lse"), (prob, "prob")):
+        _need(t, n)
+    C, d = h.shape
+    V = emb.shape[0]
+    if prob is None:
+        prob = torch.empty(C, dtype=torch.float32, device=h.device)
+    rc = load().dg_token_prob(_ptr(h), _ptr(emb), _ptr(tokens), _ptr(lse), _ptr(prob), C, V, d, _dtype_code(h),
+                              _stream(stream))
+    _check("dg_token_prob", rc)
+    return prob
+
+
+def unmask(tokens, argmax, conf, mask_id, threshold, unmasked=None, stream=None):
+    for t, n in ((tokens, "tokens"), (argmax, "argmax"), (conf, "conf"), (unmasked, "unmasked")):
+        _need(t, n)
+    rc = load().dg_unmask(_ptr(tokens), _ptr(argmax), _ptr(conf), tokens.shape[0], int(mask_id), float(threshold),
+                          _ptr(unmasked), _stream(stream))
+    _check("dg_unmask", rc)
+    return tokens
+
+
+def canvas_fill(tokens, value, stream=None):
+    _need(tokens, "tokens")
+    rc = load().dg_canvas_fill(_ptr(tokens), tokens.shape[0], int(value), _stream(stream))
+    _check("dg_canvas_fill", rc)
+    return tokens
+
+
+def count_flags(flags, count=None, stream=None):
+    """Device-side count of non-zero flags (an int32 tensor of one element)."""
+    _need(flags, "flags")
+    if count is None:
+        count = torch.empty(1, dtype=torch.int32, device=flags.device)
+    rc = load().dg_count_flags(_ptr(flags), flags.shape[0], _ptr(count), _stream(stream))
+    _check("dg_count_flags", rc)
+    return count

@@ -8,6 +8,16 @@ Each step runs, on one stream and entirely in libdgcanvas kernels:
                          and the threshold re-noise of low-confidence positions
 and each canvas starts with dg_canvas_init and ends with dg_kv_append.
 
+Variants (explainer, "1. Masked diffusion" and "Self-conditioning"):
+  mask_id=...            masked diffusion: the canvas starts as [MASK]
+                         (dg_canvas_fill) and each step unmasks confident
+                         positions for good (dg_vocab_step + dg_unmask)
+  next_input()           the next step's stand-in input E[token] + S
+                         (dg_selfcond_input)
+  generate(early_stop=True)  finish a canvas at the first step that re-noises
+                         (or unmasks) nothing, counted on the device
+                         (dg_count_flags)
+
 The backbone that turns tokens into Q/K/V and the final hidden state is not
 part of this path; `backbone(block, step, tokens, selfcond)` supplies them
 (the tests and the benchmark use seeded synthetic tensors).
@@ -36,7 +46,7 @@ class CanvasDenoiser:
     """Owns the device buffers of one canvas stream (cache, canvas, outputs,
     workspaces) and issues the C-ABI calls of each step."""
 
-    def __init__(self, emb, k_cache, v_cache, prefix_len, C, Hq, threshold, seed, stream=None):
+    def __init__(self, emb, k_cache, v_cache, prefix_len, C, Hq, threshold, seed, stream=None, mask_id=None):
         self.emb, self.k_cache, self.v_cache = emb, k_cache, v_cache
         self.Hkv, self.cap, self.hd = k_cache.shape
         self.V, self.d = emb.shape
@@ -45,6 +55,7 @@ class CanvasDenoiser:
         self.threshold = float(threshold)
         self.seed = int(seed)
         self.stream = stream
+        self.mask_id = mask_id
         dev, dt = emb.device, emb.dtype
         code = B.DG_BF16 if dt == torch.bfloat16 else B.DG_F32
         self.tokens = torch.empty(C, dtype=torch.int32, device=dev)
@@ -56,6 +67,8 @@ class CanvasDenoiser:
             lse=torch.empty(C, dtype=torch.float32, device=dev),
             selfcond=torch.empty((C, self.d), dtype=dt, device=dev),
             renoised=torch.empty(C, dtype=torch.uint8, device=dev))
+        self.count = torch.zeros(1, dtype=torch.int32, device=dev)
+        self.x = torch.empty((C, self.d), dtype=dt, device=dev)
         # workspaces sized for the longest prefix this cache can hold
         wa = max(B.canvas_attn_workspace_size(C, Hq, self.Hkv, self.hd, p, code)
                  for p in (self.len, max(self.len, self.cap - C)))
@@ -64,18 +77,38 @@ class CanvasDenoiser:
                                     device=dev)
 
     def begin_canvas(self):
-        """A fresh canvas of uniform random tokens at absolute positions [len, len + C)."""
-        B.canvas_init(self.tokens, self.V, self.seed, self.len, stream=self.stream)
+        """A fresh canvas of uniform random tokens at absolute positions [len, len + C)
+        (masked diffusion: every position [MASK])."""
+        if self.mask_id is not None:
+            B.canvas_fill(self.tokens, self.mask_id, stream=self.stream)
+        else:
+            B.canvas_init(self.tokens, self.V, self.seed, self.len, stream=self.stream)
 
     def step(self, step, q, k_canvas, v_canvas, h):
         o = self.out
         B.canvas_attn(q, self.k_cache, self.v_cache, self.len, k_canvas, v_canvas, out=o.attn_out, lse=o.attn_lse,
                       workspace=self.ws_attn, stream=self.stream)
+        if self.mask_id is not None:
+            B.vocab_step(h, self.emb, argmax=o.argmax, conf=o.conf, lse=o.lse, selfcond=o.selfcond,
+                         workspace=self.ws_vocab, stream=self.stream)
+            B.unmask(self.tokens, o.argmax, o.conf, self.mask_id, self.threshold, unmasked=o.renoised,
+                     stream=self.stream)
+            return o
         # vocabulary step with the threshold re-noise fused into its last kernel
         B.vocab_step_renoise(h, self.emb, self.tokens, self.threshold, self.seed, step, self.len, argmax=o.argmax,
                              conf=o.conf, lse=o.lse, selfcond=o.selfcond, renoised=o.renoised,
                              workspace=self.ws_vocab, stream=self.stream)
         return o
+
+    def changed_positions(self) -> int:
+        """Positions the last step re-noised (masked diffusion: unmasked),
+        counted on the device; reading it synchronises the stream."""
+        B.count_flags(self.out.renoised, count=self.count, stream=self.stream)
+        return int(self.count.item())
+
+    def next_input(self):
+        """The next step's stand-in input x = E[token] + S (self-conditioning)."""
+        return B.selfcond_input(self.tokens, self.emb, self.out.selfcond, x=self.x, stream=self.stream)
 
     def end_canvas(self, k_final, v_final, q_final=None):
         """Incremental causal prefill of the finished canvas: append its K/V."""
@@ -85,17 +118,25 @@ class CanvasDenoiser:
         return out, lse
 
 
-def generate(denoiser: CanvasDenoiser, n_blocks: int, steps: int, backbone, on_step=None):
-    """Block diffusion: for each block, `steps` denoising steps then an append.
-    Returns the finished canvases' tokens (list of int32 device tensors)."""
+def generate(denoiser: CanvasDenoiser, n_blocks: int, steps: int, backbone, on_step=None, early_stop=False):
+    """Block diffusion: for each block, up to `steps` denoising steps then an
+    append (early_stop: the canvas ends after the first step that changed no
+    position). Returns the finished canvases' tokens (list of int32 device
+    tensors); `denoiser.steps_taken` lists the steps each canvas ran."""
     finished = []
+    denoiser.steps_taken = []
     for b in range(n_blocks):
         denoiser.begin_canvas()
+        ran = 0
         for s in range(steps):
             q, kc, vc, h = backbone(b, s, denoiser.tokens, denoiser.out.selfcond)
             denoiser.step(s, q, kc, vc, h)
+            ran = s + 1
             if on_step is not None:
                 on_step(b, s, denoiser)
+            if early_stop and denoiser.changed_positions() == 0:
+                break
+        denoiser.steps_taken.append(ran)
         finished.append(denoiser.tokens.clone())
         q, kc, vc, _ = backbone(b, steps, denoiser.tokens, denoiser.out.selfcond)
         denoiser.end_canvas(kc, vc)

@@ -24,7 +24,7 @@ import torch
 
 _PURPOSES = {
     "emb": 1, "k_prefix": 2, "v_prefix": 3, "q": 4, "k_canvas": 5, "v_canvas": 6,
-    "h_noise": 7, "targets": 8, "tokens": 9, "misc": 10,
+    "h_noise": 7, "targets": 8, "tokens": 9, "misc": 10, "selfcond": 11, "h": 12,
 }
 
 

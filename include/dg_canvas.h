@@ -185,6 +185,54 @@ DG_API int dg_kv_append(void* k_cache, void* v_cache, int64_t cap, int64_t* len,
                  const void* q_new, int Hq, void* out, float* lse,
                  void* workspace, size_t workspace_bytes, void* stream);
 
+/* ---------------------------------------------------------------- next to the step
+ * Self-conditioning input. DiffusionGemma explainer, "Self-conditioning": the
+ * probabilities times the embedding table (selfcond, from dg_vocab_step) are
+ * handed to the next step. The backbone layer that takes them is outside this
+ * library; this is the stand-in input it would read:
+ *   x[i][:] = emb[tokens[i]][:] + selfcond[i][:]    (selfcond NULL: emb rows alone)
+ * summed in fp32 and rounded once to dtype.
+ *   tokens [C] int32   emb [V][d] (dtype)   selfcond [C][d] (dtype) or NULL
+ *   x [C][d] (dtype, out; must not alias the inputs)
+ * Requirements: C >= 1, V >= 1, d >= 1 with d % 8 == 0 (DG_BF16) or d % 4 == 0
+ * (DG_F32); every pointer 16-byte aligned. A token outside [0, V) gives a zero
+ * row and latches DG_ERR_DEVICE_BOUNDS.
+ */
+DG_API int dg_selfcond_input(const int32_t* tokens, const void* emb, const void* selfcond, void* x, int C, int V,
+                             int d, int dtype, void* stream);
+
+/* Probability of the token now on the canvas. DiffusionGemma explainer,
+ * "2. Uniform-state diffusion", with "a token's probability" read as the
+ * probability of the current token rather than of the prediction:
+ *   prob[i] = exp(h[i] . emb[tokens[i]] - lse[i])
+ * where lse is the natural-log log-sum-exp dg_vocab_step returned for row i
+ * (fp32 dot product). Passing prob to dg_renoise as conf re-noises by this
+ * reading.
+ *   h [C][d] (dtype)   emb [V][d] (dtype)   tokens [C] int32   lse [C] fp32
+ *   prob [C] fp32 (out)
+ * Requirements: as dg_selfcond_input. A token outside [0, V) gives prob 0 and
+ * latches DG_ERR_DEVICE_BOUNDS.
+ */
+DG_API int dg_token_prob(const void* h, const void* emb, const int32_t* tokens, const float* lse, float* prob, int C,
+                         int V, int d, int dtype, void* stream);
+
+/* Masked diffusion with lock-in. DiffusionGemma explainer, "1. Masked
+ * diffusion": positions start as a [MASK] id; once the model is confident a
+ * [MASK] becomes a word, and a replaced token is never changed again:
+ *   if tokens[i] == mask_id and conf[i] >= threshold (fp32):
+ *        tokens[i] = argmax[i], unmasked[i] = 1
+ *   else tokens[i] unchanged,   unmasked[i] = 0          (unmasked may be NULL)
+ */
+DG_API int dg_unmask(int32_t* tokens, const int32_t* argmax, const float* conf, int C, int32_t mask_id,
+                     float threshold, uint8_t* unmasked, void* stream);
+
+/* tokens[i] = value for i < C (e.g. a fully masked canvas for dg_unmask). */
+DG_API int dg_canvas_fill(int32_t* tokens, int C, int32_t value, void* stream);
+
+/* *count = number of i < C with flags[i] != 0, written on the device (early
+ * stop: a step whose renoised flags are all zero finishes the canvas). */
+DG_API int dg_count_flags(const uint8_t* flags, int C, int32_t* count, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -22,3 +22,4 @@ from .attention import canvas_attention  # noqa: F401
 from .vocab import vocab_step  # noqa: F401
 from .renoise import renoise, canvas_init  # noqa: F401
 from .kv import kv_append  # noqa: F401
+from .variants import selfcond_input, token_prob, unmask, canvas_fill, finished_early  # noqa: F401

@@ -31,9 +31,8 @@ import numpy as np
 def selfcond_input(tokens, emb, selfcond=None):
     """x [C][d] float64: the embedding row of each canvas token plus its
     self-conditioning vector (None: the embedding rows alone)."""
-    E = np.asarray(emb, dtype=np.float64)
     tok = np.asarray(tokens, dtype=np.int64)
-    x = E[tok].copy()
+    x = np.asarray(emb)[tok].astype(np.float64)  # the C gathered rows, then widened
     if selfcond is not None:
         x += np.asarray(selfcond, dtype=np.float64)
     return x
@@ -43,9 +42,9 @@ def token_prob(h, emb, tokens, lse):
     """p [C] float64: the softmax probability of token_i in row i, given that
     row's log-sum-exp (natural log)."""
     H = np.asarray(h, dtype=np.float64)
-    E = np.asarray(emb, dtype=np.float64)
     tok = np.asarray(tokens, dtype=np.int64)
-    logit = np.einsum("ij,ij->i", H, E[tok])
+    Et = np.asarray(emb)[tok].astype(np.float64)
+    logit = np.einsum("ij,ij->i", H, Et)
     return np.exp(logit - np.asarray(lse, dtype=np.float64))
 
 

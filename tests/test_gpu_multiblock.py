@@ -68,3 +68,65 @@ def test_generate_matches_oracle_each_step(lib, C, V, d, Hq, Hkv, P0, blocks, st
     np.testing.assert_array_equal(_np(k_d), mirror["k"])
     np.testing.assert_array_equal(_np(v_d), mirror["v"])
     assert stats["flagged"] <= FLAG_BUDGET * stats["total"]
+
+
+def test_masked_diffusion_steps_match_oracle(lib):
+    """Masked diffusion through the driver: a [MASK] canvas, each step unmasks
+    the confident positions for good; checked step by step (teacher-forced)."""
+    C, V, d, Hq, Hkv, hd, P0, steps = 128, 8192, 256, 4, 2, 128, 256, 4
+    thr, seed, alpha, mask_id = 0.3, 11, 6.0, V - 1
+    emb = synth.embedding(V, d, seed, std=0.1)
+    k, v = synth.kv_prefix(Hkv, P0 + C, hd, P0, seed)
+    den = CanvasDenoiser(emb.cuda(), k.cuda(), v.cuda(), P0, C, Hq, thr, seed, mask_id=mask_id)
+    state = {"tok": np.full(C, mask_id, np.int32)}
+    inputs = {}
+
+    def backbone(b, s, tokens, selfcond):
+        q, kc, vc = synth.canvas_qkv(C, Hq, Hkv, hd, seed, block=b, step=s)
+        h = synth.hidden(emb, synth.targets(C, V, seed, block=b), alpha * (s + 1) / steps, seed, block=b, step=s)
+        inputs[(b, s)] = h
+        return q.cuda(), kc.cuda(), vc.cuda(), h.cuda()
+
+    def on_step(b, s, dn):
+        rv = oracle.vocab_step(_np(inputs[(b, s)]), _np(emb))
+        ref, _ = oracle.unmask(state["tok"], rv["argmax"], rv["conf"].astype(np.float32), mask_id, thr)
+        got = _np(dn.tokens)
+        fl = decision_flags(rv, thr)
+        assert ((got == ref) | fl).all(), f"masked tokens step {s}"
+        # locked: a position that held a word keeps it
+        held = state["tok"] != mask_id
+        np.testing.assert_array_equal(got[held], state["tok"][held])
+        state["tok"] = got  # teacher-forced: the oracle continues from the GPU's canvas
+
+    generate(den, 1, steps, backbone, on_step=on_step)
+    assert (state["tok"] != mask_id).sum() > 0
+
+
+def test_early_stop_and_next_input(lib):
+    """A canvas whose positions are all confident re-noises nothing at its
+    first step, so early stop finishes it after one step; the next input is
+    E[token] + S."""
+    C, V, d, Hq, Hkv, hd, P0 = 64, 4096, 128, 4, 2, 128, 128
+    thr, seed = 0.3, 3
+    emb = synth.embedding(V, d, seed, std=0.3)
+    k, v = synth.kv_prefix(Hkv, P0 + 2 * C, hd, P0, seed)
+    den = CanvasDenoiser(emb.cuda(), k.cuda(), v.cuda(), P0, C, Hq, thr, seed)
+    seen = {}
+
+    def backbone(b, s, tokens, selfcond):
+        q, kc, vc = synth.canvas_qkv(C, Hq, Hkv, hd, seed, block=b, step=s)
+        alpha = 200.0 if b == 0 else 0.0  # block 0 certain, block 1 uniform
+        h = synth.hidden(emb, synth.targets(C, V, seed, block=b), alpha, seed, block=b, step=s)
+        seen[(b, s)] = h
+        return q.cuda(), kc.cuda(), vc.cuda(), h.cuda()
+
+    def on_step(b, s, dn):
+        rv = oracle.vocab_step(_np(seen[(b, s)]), _np(emb))
+        _, rn = oracle.renoise(rv["argmax"], rv["conf"].astype(np.float32), V, thr, seed, s, dn.len)
+        assert dn.changed_positions() == int(rn.sum())
+        x = dn.next_input()
+        ref = oracle.selfcond_input(_np(dn.tokens), _np(emb), _np(dn.out.selfcond))
+        assert_rows_close(_np(x), ref, what="next input")
+
+    generate(den, 2, 3, backbone, on_step=on_step, early_stop=True)
+    assert den.steps_taken == [1, 3]

@@ -1,0 +1,136 @@
+"""GPU parity for the rows next to the step (self-conditioning input,
+probability of the current token, masked-diffusion unmasking, canvas fill,
+flag count, early stop) and for prompt-prefill shapes of the causal append,
+against the float64 oracle on the same seeded bytes."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from canvas_denoising_gb300 import binding as B
+from canvas_denoising_gb300 import synth
+from tests.parity import CONF_REL, LSE_ABS, assert_rows_close
+
+pytestmark = pytest.mark.gpu
+
+
+def _np(t):
+    return t.detach().float().cpu().numpy() if t.dtype in (torch.bfloat16, torch.float16) else t.detach().cpu().numpy()
+
+
+def _bf16_of(x64):
+    """float64 -> bf16 values (round to nearest even through float32, which is
+    exact here: a sum of two bf16 numbers fits in float32)."""
+    return torch.from_numpy(np.asarray(x64, np.float32)).to(torch.bfloat16).float().numpy()
+
+
+# ------------------------------------------------------------------ self-conditioning input
+@pytest.mark.parametrize("C,V,d", [(256, 32768, 2816), (100, 1000, 264), (1, 64, 8)])
+def test_selfcond_input_bf16(lib, C, V, d):
+    emb = synth.embedding(V, d, seed=1)
+    sc = synth.normal((C, d), seed=1, purpose="selfcond", std=0.02)
+    tok = synth.randint(V, (C,), seed=1, purpose="tokens").to(torch.int32)
+    x = B.selfcond_input(tok.cuda(), emb.cuda(), sc.cuda())
+    ref = oracle.selfcond_input(tok.numpy(), _np(emb), _np(sc))
+    assert_rows_close(_np(x), ref, what="selfcond input")
+    exact = (_np(x) == _bf16_of(ref)).mean()
+    assert exact >= 0.999, f"only {exact:.4%} of elements equal the rounded oracle sum"
+    # without S: the embedding rows, bytewise
+    x0 = B.selfcond_input(tok.cuda(), emb.cuda())
+    assert x0.cpu().view(torch.int16).numpy().tobytes() == emb[tok.long()].view(torch.int16).numpy().tobytes()
+    assert B.device_status() == B.DG_OK
+
+
+def test_selfcond_input_f32_and_bad_token(lib):
+    C, V, d = 33, 500, 36
+    emb = synth.embedding(V, d, seed=2, dtype=torch.float32)
+    sc = synth.normal((C, d), seed=2, purpose="selfcond", dtype=torch.float32)
+    tok = synth.randint(V, (C,), seed=2, purpose="tokens").to(torch.int32)
+    x = B.selfcond_input(tok.cuda(), emb.cuda(), sc.cuda())
+    np.testing.assert_allclose(_np(x), oracle.selfcond_input(tok.numpy(), _np(emb), _np(sc)), rtol=1e-6, atol=1e-7)
+    assert B.device_status() == B.DG_OK
+    tok[5] = V  # out of range: a zero row and a latched bounds error
+    x = B.selfcond_input(tok.cuda(), emb.cuda(), sc.cuda())
+    assert B.device_status() == B.DG_ERR_DEVICE_BOUNDS
+    assert (_np(x)[5] == 0).all()
+
+
+# ------------------------------------------------------------------ probability of the current token
+@pytest.mark.parametrize("C,V,d,alpha", [(256, 32768, 1024, 26.0), (200, 9000, 320, 6.0)])
+def test_token_prob_end_to_end(lib, C, V, d, alpha):
+    emb = synth.embedding(V, d, seed=3)
+    tgt = synth.targets(C, V, seed=3)
+    h = synth.hidden(emb, tgt, alpha, seed=3)
+    am, conf, lse, _ = B.vocab_step(h.cuda(), emb.cuda())
+    tok = synth.randint(V, (C,), seed=3, purpose="tokens").to(torch.int32)
+    tok[::3] = tgt[::3].to(torch.int32)  # some rows hold the likely token
+    prob = B.token_prob(h.cuda(), emb.cuda(), tok.cuda(), lse)
+    ref_v = oracle.vocab_step(_np(h), _np(emb), want_top2=False)
+    ref = oracle.token_prob(_np(h), _np(emb), tok.numpy(), ref_v["lse"])
+    # lse within 1e-2 absolute bounds the relative error of exp(logit - lse)
+    np.testing.assert_allclose(_np(prob), ref, rtol=CONF_REL, atol=1e-30)
+    # the argmax's probability is the confidence
+    p_am = B.token_prob(h.cuda(), emb.cuda(), am, lse)
+    np.testing.assert_allclose(_np(p_am), _np(conf), rtol=1e-4)
+    assert B.device_status() == B.DG_OK
+
+
+def test_token_prob_kernel_alone_f32(lib):
+    C, V, d = 40, 700, 52
+    emb = synth.embedding(V, d, seed=4, dtype=torch.float32, std=0.3)
+    h = synth.normal((C, d), seed=4, purpose="h", dtype=torch.float32)
+    tok = synth.randint(V, (C,), seed=4, purpose="tokens").to(torch.int32)
+    ref_v = oracle.vocab_step(_np(h), _np(emb), want_top2=False)
+    lse = torch.from_numpy(ref_v["lse"].astype(np.float32))
+    prob = B.token_prob(h.cuda(), emb.cuda(), tok.cuda(), lse.cuda())
+    np.testing.assert_allclose(_np(prob), oracle.token_prob(_np(h), _np(emb), tok.numpy(), lse.numpy()), rtol=1e-5)
+
+
+# ------------------------------------------------------------------ masked diffusion, fill, count
+@pytest.mark.parametrize("C,thr", [(256, 0.5), (1000, 0.3), (7, 0.0), (256, 1.5)])
+def test_unmask_bit_exact(lib, C, thr):
+    g = torch.Generator().manual_seed(C)
+    mask_id = 262143
+    tok = torch.randint(0, 1000, (C,), generator=g, dtype=torch.int32)
+    tok[torch.rand(C, generator=g) < 0.6] = mask_id
+    am = torch.randint(0, 1000, (C,), generator=g, dtype=torch.int32)
+    conf = torch.rand(C, generator=g, dtype=torch.float32)
+    conf[: min(5, C)] = thr if thr <= 1 else 0.5  # equality unmasks
+    td = tok.cuda()
+    flags = torch.zeros(C, dtype=torch.uint8, device="cuda")
+    B.unmask(td, am.cuda(), conf.cuda(), mask_id, thr, unmasked=flags)
+    ref_tok, ref_flag = oracle.unmask(tok.numpy(), am.numpy(), conf.numpy(), mask_id, thr)
+    np.testing.assert_array_equal(_np(td), ref_tok)
+    np.testing.assert_array_equal(_np(flags), ref_flag)
+    cnt = B.count_flags(flags)
+    assert int(cnt.item()) == int(ref_flag.sum())
+
+
+def test_canvas_fill_and_count(lib):
+    for C in (1, 256, 1000):
+        tok = torch.empty(C, dtype=torch.int32, device="cuda")
+        B.canvas_fill(tok, 262143)
+        np.testing.assert_array_equal(_np(tok), oracle.canvas_fill(C, 262143))
+        f = (torch.arange(C, device="cuda") % 3 == 0).to(torch.uint8)
+        assert int(B.count_flags(f).item()) == (C + 2) // 3
+        z = torch.zeros(C, dtype=torch.uint8, device="cuda")
+        assert int(B.count_flags(z).item()) == 0 and oracle.finished_early(_np(z))
+
+
+# ------------------------------------------------------------------ prompt prefill shapes
+@pytest.mark.parametrize("P,C", [(0, 2048), (1024, 2048), (0, 520)])
+def test_prefill_shapes_causal_append(lib, P, C):
+    """Incremental causal prefill of a whole prompt chunk (the step before the
+    denoising loop): a C-row block appended at P, with its causal attention."""
+    Hkv, Hq, hd = 8, 16, 128
+    cap = P + C
+    k, v = synth.kv_prefix(Hkv, cap, hd, P, seed=5)
+    q, kn, vn = synth.canvas_qkv(C, Hq, Hkv, hd, seed=5)
+    kd, vd = k.cuda(), v.cuda()
+    n, out, lse = B.kv_append(kd, vd, P, kn.cuda(), vn.cuda(), q_new=q.cuda())
+    assert n == P + C
+    assert kd[:, P:P + C].cpu().view(torch.int16).numpy().tobytes() == kn.view(torch.int16).numpy().tobytes()
+    ro, rl = oracle.canvas_attention(_np(q), _np(k), _np(v), P, _np(kn), _np(vn), causal=True)
+    assert_rows_close(_np(out).reshape(C * Hq, hd), ro.reshape(C * Hq, hd), what="prefill out")
+    assert np.abs(_np(lse) - rl).max() <= LSE_ABS
+    assert B.device_status() == B.DG_OK
