@@ -48,6 +48,12 @@ _SIGS = {
     "dg_unmask": (_c_int, [_p, _p, _p, _c_int, ctypes.c_int32, _c_f, _p, _p]),
     "dg_canvas_fill": (_c_int, [_p, _c_int, ctypes.c_int32, _p]),
     "dg_count_flags": (_c_int, [_p, _c_int, _p, _p]),
+    "dg_canvas_attn_devlen": (_c_int, [_p, _p, _p, _c_i64, _p, _c_i64, _p, _p, _p, _p, _c_int, _c_int, _c_int, _c_int,
+                                       _c_f, _c_int, _c_int, _p, _c_sz, _p]),
+    "dg_canvas_init_devpos": (_c_int, [_p, _c_int, _c_int, _c_u64, _p, _p]),
+    "dg_vocab_step_renoise_devpos": (_c_int, [_p, _p, _c_int, _c_int, _c_int, _c_int, _p, _p, _p, _p, _p, _c_f,
+                                              _c_u64, _c_u32, _p, _p, _p, _c_sz, _p]),
+    "dg_kv_append_devlen": (_c_int, [_p, _p, _c_i64, _p, _p, _p, _c_int, _c_int, _c_int, _c_int, _p]),
 }
 
 EXPORTS = tuple(_SIGS)
@@ -327,3 +333,55 @@ def count_flags(flags, count=None, stream=None):
     rc = load().dg_count_flags(_ptr(flags), flags.shape[0], _ptr(count), _stream(stream))
     _check("dg_count_flags", rc)
     return count
+
+
+# ------------------------------------------------------------------ device-side cache length
+def canvas_attn_devlen(q, k_cache, v_cache, prefix_len_dev, prefix_max, k_canvas, v_canvas, out=None, lse=None,
+                       scale=-1.0, mask=DG_MASK_BIDIR, workspace=None, stream=None):
+    """dg_canvas_attn with the prefix length in a device int64 tensor of one element."""
+    for t, n in ((q, "q"), (k_cache, "k_cache"), (v_cache, "v_cache"), (k_canvas, "k_canvas"),
+                 (v_canvas, "v_canvas"), (prefix_len_dev, "prefix_len_dev")):
+        _need(t, n)
+    C, Hq, hd = q.shape
+    Hkv, cap = k_cache.shape[0], k_cache.shape[1]
+    dt = _dtype_code(q)
+    out = torch.empty_like(q) if out is None else out
+    lse = torch.empty((Hq, C), dtype=torch.float32, device=q.device) if lse is None else lse
+    need = canvas_attn_workspace_size(C, Hq, Hkv, hd, prefix_max, dt)
+    if workspace is None and need:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    rc = load().dg_canvas_attn_devlen(_ptr(q), _ptr(k_cache), _ptr(v_cache), cap, _ptr(prefix_len_dev), prefix_max,
+                                      _ptr(k_canvas), _ptr(v_canvas), _ptr(out), _ptr(lse), C, Hq, Hkv, hd,
+                                      float(scale), dt, mask, _ptr(workspace), ws_bytes, _stream(stream))
+    _check("dg_canvas_attn_devlen", rc)
+    return out, lse
+
+
+def canvas_init_devpos(tokens, V, seed, abs_pos0_dev, stream=None):
+    _need(tokens, "tokens")
+    rc = load().dg_canvas_init_devpos(_ptr(tokens), tokens.shape[0], V, seed, _ptr(abs_pos0_dev), _stream(stream))
+    _check("dg_canvas_init_devpos", rc)
+    return tokens
+
+
+def vocab_step_renoise_devpos(h, emb, tokens, threshold, seed, step, abs_pos0_dev, argmax, conf, lse, selfcond,
+                              renoised, workspace, stream=None):
+    C, d = h.shape
+    V = emb.shape[0]
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    rc = load().dg_vocab_step_renoise_devpos(_ptr(h), _ptr(emb), C, V, d, _dtype_code(h), _ptr(argmax), _ptr(conf),
+                                             _ptr(lse), _ptr(selfcond), _ptr(tokens), float(threshold), seed, step,
+                                             _ptr(abs_pos0_dev), _ptr(renoised), _ptr(workspace), ws_bytes,
+                                             _stream(stream))
+    _check("dg_vocab_step_renoise_devpos", rc)
+    return tokens
+
+
+def kv_append_devlen(k_cache, v_cache, len_dev, k_new, v_new, stream=None):
+    for t, n in ((k_cache, "k_cache"), (v_cache, "v_cache"), (k_new, "k_new"), (v_new, "v_new")):
+        _need(t, n)
+    Hkv, cap, hd = k_cache.shape
+    rc = load().dg_kv_append_devlen(_ptr(k_cache), _ptr(v_cache), cap, _ptr(len_dev), _ptr(k_new), _ptr(v_new),
+                                    k_new.shape[1], Hkv, hd, _dtype_code(k_cache), _stream(stream))
+    _check("dg_kv_append_devlen", rc)

@@ -128,7 +128,7 @@ extern "C" int dg_vocab_step_renoise(const void* h, const void* emb, int C, int 
   if (!aligned16(h) || !aligned16(emb) || (selfcond && !aligned16(selfcond))) return DG_ERR_INVALID_ARG;
   if (workspace_bytes < vocab_tc_workspace(C, V, d)) return DG_ERR_WORKSPACE;
   if (vocab_tc_workspace(C, V, d) && ((uintptr_t)workspace & 255u)) return DG_ERR_INVALID_ARG;
-  RenoiseArgs rn{tokens, renoised, threshold, seed, step, abs_pos0};
+  RenoiseArgs rn{tokens, renoised, threshold, seed, step, abs_pos0, nullptr};
   return vocab_tc_launch((const __nv_bfloat16*)h, (const __nv_bfloat16*)emb, C, V, d, argmax, conf, lse,
                          (__nv_bfloat16*)selfcond, workspace, workspace_bytes, (cudaStream_t)stream, &rn);
 }
@@ -136,4 +136,39 @@ extern "C" int dg_vocab_step_renoise(const void* h, const void* emb, int C, int 
 extern "C" int dg_vocab_step_plan(int C, int V, int d, int dtype, int32_t* plan) {
   if (!plan || dtype != DG_BF16 || C < 1 || C > 256 || V < 1 || d < 64 || d % 64 || d > 8192) return DG_ERR_INVALID_ARG;
   return vocab_tc_plan(C, V, d, plan);
+}
+
+extern "C" int dg_vocab_step_renoise_devpos(const void* h, const void* emb, int C, int V, int d, int dtype,
+                                            int32_t* argmax, float* conf, float* lse, void* selfcond, int32_t* tokens,
+                                            float threshold, uint64_t seed, uint32_t step,
+                                            const int64_t* abs_pos0_dev, uint8_t* renoised, void* workspace,
+                                            size_t workspace_bytes, void* stream) {
+  if (!tokens || !abs_pos0_dev || threshold != threshold) return DG_ERR_INVALID_ARG;
+  if (dtype != DG_BF16) return DG_ERR_UNSUPPORTED;
+  if (!h || !emb || !argmax || !conf || C < 1 || V < 1 || d < 1) return DG_ERR_INVALID_ARG;
+  if (C > 256 || d % 64 || d > 8192) return DG_ERR_UNSUPPORTED;
+  if (!aligned16(h) || !aligned16(emb) || (selfcond && !aligned16(selfcond))) return DG_ERR_INVALID_ARG;
+  if (workspace_bytes < vocab_tc_workspace(C, V, d)) return DG_ERR_WORKSPACE;
+  if (vocab_tc_workspace(C, V, d) && ((uintptr_t)workspace & 255u)) return DG_ERR_INVALID_ARG;
+  RenoiseArgs rn{tokens, renoised, threshold, seed, step, 0, abs_pos0_dev};
+  return vocab_tc_launch((const __nv_bfloat16*)h, (const __nv_bfloat16*)emb, C, V, d, argmax, conf, lse,
+                         (__nv_bfloat16*)selfcond, workspace, workspace_bytes, (cudaStream_t)stream, &rn);
+}
+
+extern "C" int dg_canvas_attn_devlen(const void* q, const void* k_cache, const void* v_cache, int64_t cap,
+                                     const int64_t* prefix_len_dev, int64_t prefix_max, const void* k_canvas,
+                                     const void* v_canvas, void* out, float* lse, int C, int Hq, int Hkv, int hd,
+                                     float scale, int dtype, int mask, void* workspace, size_t workspace_bytes,
+                                     void* stream) {
+  if (!q || !prefix_len_dev || !k_canvas || !v_canvas || !out) return DG_ERR_INVALID_ARG;
+  if (prefix_max > 0 && (!k_cache || !v_cache)) return DG_ERR_INVALID_ARG;
+  if (C < 1 || Hq < 1 || Hkv < 1 || Hq % Hkv || prefix_max < 0 || prefix_max > cap) return DG_ERR_INVALID_ARG;
+  if (mask != DG_MASK_BIDIR && mask != DG_MASK_CAUSAL_BLOCK) return DG_ERR_INVALID_ARG;
+  if (dtype != DG_BF16 || hd != 128) return DG_ERR_UNSUPPORTED;
+  if (!aligned16(q) || !aligned16(k_canvas) || !aligned16(v_canvas) || !aligned16(out)) return DG_ERR_INVALID_ARG;
+  if (prefix_max > 0 && (!aligned16(k_cache) || !aligned16(v_cache))) return DG_ERR_INVALID_ARG;
+  if (workspace_bytes < attn_workspace(C, Hq, Hkv, hd, prefix_max, dtype)) return DG_ERR_WORKSPACE;
+  if (scale <= 0.f) scale = 1.0f / sqrtf((float)hd);
+  return attn_tc_launch(q, k_cache, v_cache, cap, prefix_max, k_canvas, v_canvas, out, lse, C, Hq, Hkv, scale, mask,
+                        workspace, workspace_bytes, (cudaStream_t)stream, prefix_len_dev);
 }

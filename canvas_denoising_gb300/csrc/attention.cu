@@ -434,11 +434,19 @@ int attn_combine_launch(const float* part_o, const float* part_lse, __nv_bfloat1
 size_t attn_workspace(int C, int Hq, int Hkv, int hd, int64_t P, int dtype) {
   if (dtype != DG_BF16 || C < 1 || Hkv < 1 || Hq % Hkv) return 0;
   if (hd == 128) return attn_tc_workspace(C, Hq, Hkv, P);
-  Plan pl = make_plan(C, Hq, Hkv, P);
-  if (pl.splits <= 1) return 0;
-  size_t o = (size_t)pl.splits * C * Hq * hd * sizeof(float);
+  // Sized for make_plan's split bound (non-decreasing in P) rather than this
+  // P's split count, so a workspace sized for the largest prefix serves every
+  // smaller one.
+  const int64_t base = ((int64_t)(Hq / Hkv) * C + BM - 1) / BM * Hkv;
+  const int64_t tiles = (P + C + BN - 1) / BN;
+  int64_t want = (2 * num_sms() + base - 1) / base;
+  const int64_t maxs = tiles / 2 > 0 ? tiles / 2 : 1;
+  if (want > maxs) want = maxs;
+  if (want > 64) want = 64;
+  if (want <= 1) return 0;
+  size_t o = (size_t)want * C * Hq * hd * sizeof(float);
   o = (o + 255) & ~(size_t)255;
-  return o + (size_t)pl.splits * Hq * C * sizeof(float);
+  return o + (size_t)want * Hq * C * sizeof(float);
 }
 
 int attn_launch(const void* q, const void* k_cache, const void* v_cache, int64_t cap, int64_t P,

@@ -72,7 +72,8 @@ struct TcArgs {
   __nv_bfloat16* out;
   float* lse;
   int C, Hq, Hkv, grp;
-  int64_t P;
+  int64_t P;              // cache prefix (with P_dev: its upper bound)
+  const int64_t* P_dev;   // device-side prefix length, or null
   int n_cache_tiles, n_tiles, tiles_per_split, splits;
   uint4* part_o;    // [group][split][256 rows][128] bf16 (O / l), rows as staged (swizzled 16-byte pieces)
   float* part_lse;  // [group][split][256]
@@ -153,13 +154,29 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int64_t M = (int64_t)a.grp * a.C;
   Ctl ctl{&abort_flag, a.status};
 
+  // key range: the cache prefix P (from device memory when P_dev is set; the
+  // tensor maps then span P_max rows, and rows past P are masked below)
+  int64_t P = a.P;
+  int nct = a.n_cache_tiles, ntl = a.n_tiles, tps = a.tiles_per_split;
+  if (a.P_dev) {
+    int64_t pd = *a.P_dev;
+    if (pd < 0 || pd > a.P) {
+      if (tid == 0) latch(a.status, DG_ERR_DEVICE_BOUNDS);
+      pd = pd < 0 ? 0 : a.P;
+    }
+    P = pd;
+    nct = (int)((P + kBN - 1) / kBN);
+    ntl = nct + (a.C + kBN - 1) / kBN;
+    tps = (ntl + a.splits - 1) / a.splits;
+  }
+
   // tiles of this CTA
-  int T0 = split * a.tiles_per_split;
-  int T1 = min(a.n_tiles, T0 + a.tiles_per_split);
+  int T0 = split * tps;
+  int T1 = min(ntl, T0 + tps);
   if (a.causal) {
     int64_t rmax = min64(M - 1, (int64_t)mblk * kBM + kBM - 1);
     int64_t imax = rmax / a.grp;  // last visible key: P + imax (a canvas row)
-    int last = a.n_cache_tiles + (int)(imax / kBN);
+    int last = nct + (int)(imax / kBN);
     T1 = min(T1, last + 1);
   }
   const int n = T1 > T0 ? T1 - T0 : 0;
@@ -169,8 +186,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool is_v = it & 1;
     const int t = T0 + (it >> 1);
     const int slot = it % kRing;
-    const bool cache = t < a.n_cache_tiles;
-    const int y = cache ? t * kBN : (t - a.n_cache_tiles) * kBN;
+    const bool cache = t < nct;
+    const int y = cache ? t * kBN : (t - nct) * kBN;
     const CUtensorMap* mp = cache ? (is_v ? &tv_c : &tk_c) : (is_v ? &tv_n : &tk_n);
     mbar_expect_tx(smem_addr(&ring_full[slot]), kTile);
     tma_load_3d(sbase + kOffRing + slot * kTile, mp, 0, y, g, smem_addr(&ring_full[slot]));
@@ -332,10 +349,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int jj = 0; jj < n; ++jj) {
       const int t = T0 + jj;
       int lim;
-      if (t < a.n_cache_tiles) {
-        lim = (int)min64(kBN, a.P - (int64_t)t * kBN);
+      if (t < nct) {
+        lim = (int)min64(kBN, P - (int64_t)t * kBN);
       } else {
-        const int64_t c0 = (int64_t)(t - a.n_cache_tiles) * kBN;
+        const int64_t c0 = (int64_t)(t - nct) * kBN;
         lim = (int)min64(kBN, a.C - c0);
         if (a.causal) lim = (int)min64(lim, i - c0 + 1);
       }
@@ -458,7 +475,19 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int grp_id = g * gridDim.x + mblk;
   const int cs = a.splits;
   constexpr int kRowPieces = kHD / 8;  // 16-byte pieces of a staged row
-  {
+  bool merge = false;
+  if (cs == 1) {
+    // one split: the staged rows are the output (bf16 O / l); coalesced copy-out
+    for (int item = tid; item < kBM * kRowPieces; item += kThreads) {
+      const int row = item / kRowPieces, pc = item % kRowPieces;
+      const int64_t R = (int64_t)mblk * kBM + row;
+      if (R >= M) continue;
+      const int64_t i = R / a.grp, h = (int64_t)g * a.grp + R % a.grp;
+      *reinterpret_cast<uint4*>(a.out + (i * a.Hq + h) * kHD + pc * 8) =
+          *reinterpret_cast<const uint4*>(sm + stage_off(row, pc));
+      if (pc == 0 && a.lse) a.lse[h * a.C + i] = s_lse[row];
+    }
+  } else {
     if (tid == 0) {
       bulk_store(a.part_o + ((size_t)grp_id * cs + split) * (kBM * kRowPieces), sbase, kBM * kStageRow);
       bulk_commit();
@@ -484,14 +513,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       s_go = go;
     }
     __syncthreads();
+    merge = s_go;
   }
-  if (s_go) {
+  if (merge) {
     // Rows [r0, r0 + nr) of the group are merged by this CTA, two 16-byte
     // pieces (16 columns) per item, so that one round of loads usually covers
-    // a thread's work: the item's lse values and pieces of up to 12 splits
+    // a thread's work: the item's lse values and pieces of up to 9 splits
     // are loaded at once, then combined with weights exp(lse_s - max) (an
-    // online rescale joins further batches of 12 splits).
-    constexpr int kBatch = 12;
+    // online rescale joins further batches of 9 splits).
+    constexpr int kBatch = 9;
     constexpr int kItemsPerRow = kRowPieces / 2;
     const int rpc = (kBM + cs - 1) / cs;
     const int r0 = split * rpc;
@@ -609,11 +639,14 @@ cudaError_t prepare_kernel() {
 
 // Split plan of the tensor-core path: one wave of CTAs, one per SM (the
 // launch is cooperative, so the grid must fit on the GPU at once).
-void attn_tc_plan(int C, int Hq, int Hkv, int64_t P, int* splits, int* tiles_per_split) {
+namespace {
+int key_tiles(int C, int64_t P) { return (int)((P + kBN - 1) / kBN) + (C + kBN - 1) / kBN; }
+
+// Upper bound of the key splits for prefix P: non-decreasing in P, so a
+// workspace sized for the largest prefix also serves every smaller one.
+int max_splits(int C, int Hq, int Hkv, int64_t P) {
   const int64_t M = (int64_t)(Hq / Hkv) * C;
   const int64_t base = ((M + kBM - 1) / kBM) * Hkv;
-  const int nct = (int)((P + kBN - 1) / kBN), nvt = (C + kBN - 1) / kBN;
-  const int tiles = nct + nvt;
   static const int env_splits = [] {
     const char* v = getenv("DG_ATTN_SPLITS");  // tuning knob: force the number of key splits
     const int x = v ? atoi(v) : 0;
@@ -621,9 +654,16 @@ void attn_tc_plan(int C, int Hq, int Hkv, int64_t P, int* splits, int* tiles_per
   }();
   int want = (int)(num_sms() / base);
   if (env_splits && env_splits < want) want = env_splits;
+  const int tiles = key_tiles(C, P);
   if (want > tiles) want = tiles;
   if (want > kMaxSplits) want = kMaxSplits;
-  if (want < 1) want = 1;
+  return want < 1 ? 1 : want;
+}
+}  // namespace
+
+void attn_tc_plan(int C, int Hq, int Hkv, int64_t P, int* splits, int* tiles_per_split) {
+  const int tiles = key_tiles(C, P);
+  const int want = max_splits(C, Hq, Hkv, P);
   const int tps = (tiles + want - 1) / want;
   if (tiles_per_split) *tiles_per_split = tps;
   *splits = (tiles + tps - 1) / tps;
@@ -636,8 +676,7 @@ struct TcLayout {
   int64_t groups;
 };
 TcLayout tc_layout(int C, int Hq, int Hkv, int64_t P) {
-  int splits = 1;
-  attn_tc_plan(C, Hq, Hkv, P, &splits, nullptr);
+  const int splits = max_splits(C, Hq, Hkv, P);  // the plan's splits never exceed this
   TcLayout L;
   const int64_t M = (int64_t)(Hq / Hkv) * C;
   L.groups = ((M + kBM - 1) / kBM) * Hkv;
@@ -645,7 +684,7 @@ TcLayout tc_layout(int C, int Hq, int Hkv, int64_t P) {
   L.part_o = 0;
   L.part_lse = al((size_t)L.groups * splits * kBM * kHD * sizeof(__nv_bfloat16));
   L.arrived = L.part_lse + al((size_t)L.groups * splits * kBM * sizeof(float));
-  L.total = L.arrived + al((size_t)L.groups * sizeof(int));
+  L.total = splits > 1 ? L.arrived + al((size_t)L.groups * sizeof(int)) : 0;  // one split: no partials
   return L;
 }
 
@@ -656,12 +695,12 @@ size_t attn_tc_workspace(int C, int Hq, int Hkv, int64_t P) {
 
 int attn_tc_launch(const void* q, const void* k_cache, const void* v_cache, int64_t cap, int64_t P,
                    const void* k_canvas, const void* v_canvas, void* out, float* lse, int C, int Hq, int Hkv,
-                   float scale, int mask, void* ws, size_t ws_bytes, cudaStream_t s) {
+                   float scale, int mask, void* ws, size_t ws_bytes, cudaStream_t s, const int64_t* P_dev) {
   DG_CUDA_TRY(prepare_kernel());
   int splits, tps;
   attn_tc_plan(C, Hq, Hkv, P, &splits, &tps);
   const TcLayout L = tc_layout(C, Hq, Hkv, P);
-  if (!ws || ws_bytes < L.total || ((uintptr_t)ws & 255u)) return DG_ERR_WORKSPACE;
+  if (splits > 1 && (!ws || ws_bytes < L.total || ((uintptr_t)ws & 255u))) return DG_ERR_WORKSPACE;
   int* st = status_ptr();
   if (!st) return DG_ERR_CUDA;
   CUtensorMap tk_c, tv_c, tk_n, tv_n;
@@ -683,13 +722,14 @@ int attn_tc_launch(const void* q, const void* k_cache, const void* v_cache, int6
   a.Hkv = Hkv;
   a.grp = Hq / Hkv;
   a.P = P;
+  a.P_dev = P_dev;
   a.n_cache_tiles = (int)((P + kBN - 1) / kBN);
   a.n_tiles = a.n_cache_tiles + (C + kBN - 1) / kBN;
   a.tiles_per_split = tps;
   a.splits = splits;
-  a.part_o = (uint4*)((char*)ws + L.part_o);
-  a.part_lse = (float*)((char*)ws + L.part_lse);
-  a.arrived = (int*)((char*)ws + L.arrived);
+  a.part_o = splits > 1 ? (uint4*)((char*)ws + L.part_o) : nullptr;
+  a.part_lse = splits > 1 ? (float*)((char*)ws + L.part_lse) : nullptr;
+  a.arrived = splits > 1 ? (int*)((char*)ws + L.arrived) : nullptr;
   a.scale_log2 = scale * 1.4426950408889634f;
   a.causal = mask == DG_MASK_CAUSAL_BLOCK;
   a.q_tma = q_tma;
@@ -700,12 +740,13 @@ int attn_tc_launch(const void* q, const void* k_cache, const void* v_cache, int6
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = kSmem + 1024;
   cfg.stream = s;
+  // several splits meet on a counter, so every CTA must be resident: cooperative
   cudaLaunchAttribute at[1];
   at[0].id = cudaLaunchAttributeCooperative;
   at[0].val.cooperative = 1;
   cfg.attrs = at;
-  cfg.numAttrs = 1;
-  DG_CUDA_TRY(cudaMemsetAsync(a.arrived, 0, (size_t)L.groups * sizeof(int), s));
+  cfg.numAttrs = splits > 1 ? 1 : 0;
+  if (splits > 1) DG_CUDA_TRY(cudaMemsetAsync(a.arrived, 0, (size_t)L.groups * sizeof(int), s));
   DG_CUDA_TRY(cudaLaunchKernelEx(&cfg, attn_fwd_tc, tk_c, tv_c, tk_n, tv_n, tq, a));
   return DG_OK;
 }

@@ -79,7 +79,8 @@ int attn_combine_launch(const float* part_o, const float* part_lse, __nv_bfloat1
 void attn_tc_plan(int C, int Hq, int Hkv, int64_t P, int* splits, int* tiles_per_split);
 int attn_tc_launch(const void* q, const void* k_cache, const void* v_cache, int64_t cap, int64_t P,
                    const void* k_canvas, const void* v_canvas, void* out, float* lse, int C, int Hq, int Hkv,
-                   float scale, int mask, void* ws, size_t ws_bytes, cudaStream_t s);
+                   float scale, int mask, void* ws, size_t ws_bytes, cudaStream_t s,
+                   const int64_t* P_dev = nullptr);
 size_t attn_tc_workspace(int C, int Hq, int Hkv, int64_t P);
 
 int vocab_simt_launch(const float* h, const float* emb, int C, int V, int d, int32_t* argmax, float* conf,
@@ -92,6 +93,7 @@ struct RenoiseArgs {  // threshold re-noise fused into the vocabulary step's las
   uint64_t seed;
   uint32_t step;
   int64_t abs_pos0;
+  const int64_t* abs_pos0_dev;  // if set, the position offset is read from device memory
 };
 
 size_t vocab_tc_workspace(int C, int V, int d);

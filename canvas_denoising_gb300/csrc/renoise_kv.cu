@@ -33,15 +33,27 @@ __global__ void renoise_kernel(int32_t* __restrict__ tokens, const int32_t* __re
 }
 
 __global__ void canvas_init_kernel(int32_t* __restrict__ tokens, int C, uint32_t V, uint64_t seed,
-                                   int64_t abs_pos0) {
+                                   int64_t abs_pos0, const int64_t* __restrict__ abs_pos0_dev) {
   int i = blockIdx.x * blockDim.x + threadIdx.x;
-  if (i < C) tokens[i] = uniform_token(seed, 0, abs_pos0 + i, kDomainInit, V);
+  const int64_t p0 = abs_pos0_dev ? *abs_pos0_dev : abs_pos0;
+  if (i < C) tokens[i] = uniform_token(seed, 0, p0 + i, kDomainInit, V);
 }
 
 // rows [P, P+C) of head blockIdx.y; `vec_per_head` 16-byte vectors per head block.
+// With len_dev set, P is read from device memory (rows of `row_vecs` vectors)
+// and a block that would end past `cap` copies nothing and latches a bounds error.
 __global__ void kv_append_kernel(uint4* __restrict__ kc, uint4* __restrict__ vc, const uint4* __restrict__ kn,
                                  const uint4* __restrict__ vn, int64_t cap_vecs_per_head, int64_t dst_off_vecs,
-                                 int64_t vec_per_head) {
+                                 int64_t vec_per_head, const int64_t* __restrict__ len_dev, int64_t row_vecs,
+                                 int64_t C, int64_t cap, int* status) {
+  if (len_dev) {
+    const int64_t P = *len_dev;
+    if (P < 0 || P + C > cap) {
+      if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) latch(status, DG_ERR_DEVICE_BOUNDS);
+      return;
+    }
+    dst_off_vecs = P * row_vecs;
+  }
   const int64_t g = blockIdx.y;
   const uint4* ks = kn + g * vec_per_head;
   const uint4* vs = vn + g * vec_per_head;
@@ -54,6 +66,12 @@ __global__ void kv_append_kernel(uint4* __restrict__ kc, uint4* __restrict__ vc,
     kd[j] = a;
     vd[j] = b;
   }
+}
+
+// *len += C after an append (same bounds rule as the copy, so both agree).
+__global__ void len_advance_kernel(int64_t* len, int64_t C, int64_t cap) {
+  const int64_t P = *len;
+  if (P >= 0 && P + C <= cap) *len = P + C;
 }
 
 }  // namespace dg
@@ -76,7 +94,7 @@ extern "C" int dg_renoise(int32_t* tokens, const int32_t* argmax, const float* c
 extern "C" int dg_canvas_init(int32_t* tokens, int C, int V, uint64_t seed, int64_t abs_pos0, void* stream) {
   if (!tokens || C < 1 || V < 1 || abs_pos0 < 0) return DG_ERR_INVALID_ARG;
   cudaStream_t s = (cudaStream_t)stream;
-  canvas_init_kernel<<<(C + 255) / 256, 256, 0, s>>>(tokens, C, (uint32_t)V, seed, abs_pos0);
+  canvas_init_kernel<<<(C + 255) / 256, 256, 0, s>>>(tokens, C, (uint32_t)V, seed, abs_pos0, nullptr);
   DG_LAUNCH_CHECK();
   return DG_OK;
 }
@@ -104,7 +122,8 @@ extern "C" int dg_kv_append(void* k_cache, void* v_cache, int64_t cap, int64_t* 
   if (gx > 64) gx = 64;
   dim3 grid(gx, Hkv);
   kv_append_kernel<<<grid, 256, 0, s>>>((uint4*)k_cache, (uint4*)v_cache, (const uint4*)k_new,
-                                        (const uint4*)v_new, cap * row_vecs, P * row_vecs, vec_per_head);
+                                        (const uint4*)v_new, cap * row_vecs, P * row_vecs, vec_per_head, nullptr,
+                                        row_vecs, C, cap, nullptr);
   DG_LAUNCH_CHECK();
   if (q_new) {
     // The block's causal attention over the updated cache: keys [0, P) from the
@@ -114,5 +133,40 @@ extern "C" int dg_kv_append(void* k_cache, void* v_cache, int64_t cap, int64_t* 
     if (rc != DG_OK) return rc;
   }
   *len = P + C;
+  return DG_OK;
+}
+
+extern "C" int dg_canvas_init_devpos(int32_t* tokens, int C, int V, uint64_t seed, const int64_t* abs_pos0_dev,
+                                     void* stream) {
+  if (!tokens || !abs_pos0_dev || C < 1 || V < 1) return DG_ERR_INVALID_ARG;
+  cudaStream_t s = (cudaStream_t)stream;
+  canvas_init_kernel<<<(C + 255) / 256, 256, 0, s>>>(tokens, C, (uint32_t)V, seed, 0, abs_pos0_dev);
+  DG_LAUNCH_CHECK();
+  return DG_OK;
+}
+
+extern "C" int dg_kv_append_devlen(void* k_cache, void* v_cache, int64_t cap, int64_t* len_dev, const void* k_new,
+                                   const void* v_new, int C, int Hkv, int hd, int dtype, void* stream) {
+  if (!k_cache || !v_cache || !len_dev || !k_new || !v_new) return DG_ERR_INVALID_ARG;
+  if (C < 1 || Hkv < 1 || cap < C) return DG_ERR_INVALID_ARG;
+  if (dtype != DG_BF16 && dtype != DG_F32) return DG_ERR_INVALID_ARG;
+  if (hd != 32 && hd != 64 && hd != 128) return DG_ERR_UNSUPPORTED;
+  if (!aligned16(k_cache) || !aligned16(v_cache) || !aligned16(k_new) || !aligned16(v_new))
+    return DG_ERR_INVALID_ARG;
+  int* st = status_ptr();
+  if (!st) return DG_ERR_CUDA;
+  cudaStream_t s = (cudaStream_t)stream;
+  const int64_t esz = dtype == DG_BF16 ? 2 : 4;
+  const int64_t row_vecs = (int64_t)hd * esz / 16;
+  const int64_t vec_per_head = (int64_t)C * row_vecs;
+  int gx = (int)((vec_per_head + 255) / 256);
+  if (gx > 64) gx = 64;
+  dim3 grid(gx, Hkv);
+  kv_append_kernel<<<grid, 256, 0, s>>>((uint4*)k_cache, (uint4*)v_cache, (const uint4*)k_new,
+                                        (const uint4*)v_new, cap * row_vecs, 0, vec_per_head, len_dev, row_vecs, C,
+                                        cap, st);
+  DG_LAUNCH_CHECK();
+  len_advance_kernel<<<1, 1, 0, s>>>(len_dev, C, cap);
+  DG_LAUNCH_CHECK();
   return DG_OK;
 }

@@ -165,6 +165,7 @@ struct Params {
   uint64_t rn_seed;
   uint32_t rn_step;
   int64_t rn_pos0;
+  const int64_t* rn_pos0_dev;  // device-side position offset (or null)
   int* status;
 };
 
@@ -704,7 +705,8 @@ __global__ void __launch_bounds__(256) vocab_combine(const Params p, const __nv_
     if (p.rn_tokens) {
       // threshold re-noise of this position (same rule and draw as dg_renoise)
       const bool low = out_conf < p.rn_threshold;
-      p.rn_tokens[i] = low ? uniform_token(p.rn_seed, p.rn_step, p.rn_pos0 + i, kDomainRenoise, (uint32_t)p.V) : ai;
+      const int64_t pos0 = p.rn_pos0_dev ? *p.rn_pos0_dev : p.rn_pos0;
+      p.rn_tokens[i] = low ? uniform_token(p.rn_seed, p.rn_step, pos0 + i, kDomainRenoise, (uint32_t)p.V) : ai;
       if (p.rn_flags) p.rn_flags[i] = low ? 1 : 0;
     }
   }
@@ -775,6 +777,7 @@ int vocab_tc_launch(const __nv_bfloat16* h, const __nv_bfloat16* emb, int C, int
   p.rn_seed = rn ? rn->seed : 0;
   p.rn_step = rn ? rn->step : 0;
   p.rn_pos0 = rn ? rn->abs_pos0 : 0;
+  p.rn_pos0_dev = rn ? rn->abs_pos0_dev : nullptr;
   DG_CUDA_TRY(cudaMemsetAsync(flags, 0, L.flag_bytes, s));
 
   const size_t smem = (size_t)kStages * kStageBytes + 1024;

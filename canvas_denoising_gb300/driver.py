@@ -141,3 +141,85 @@ def generate(denoiser: CanvasDenoiser, n_blocks: int, steps: int, backbone, on_s
         q, kc, vc, _ = backbone(b, steps, denoiser.tokens, denoiser.out.selfcond)
         denoiser.end_canvas(kc, vc)
     return finished
+
+
+class GraphedBlockDiffusion:
+    """Block diffusion with the cache length on the device: one CUDA graph per
+    canvas (init, `steps` denoising steps, append), replayed for every block
+    while the prefix grows (explainer, "Multi-canvas sampling (block
+    diffusion)"). The backbone's per-step tensors are read from fixed buffers,
+    which the caller fills before each replay (`load_block`)."""
+
+    def __init__(self, emb, k_cache, v_cache, prefix_len, C, Hq, threshold, seed, steps, stream):
+        self.emb, self.k_cache, self.v_cache = emb, k_cache, v_cache
+        self.Hkv, self.cap, self.hd = k_cache.shape
+        self.V, self.d = emb.shape
+        self.C, self.Hq, self.steps = C, Hq, steps
+        self.threshold, self.seed, self.stream = float(threshold), int(seed), stream
+        self.prefix_max = self.cap - C
+        dev, dt = emb.device, emb.dtype
+        self.len = int(prefix_len)
+        self.len_dev = torch.tensor([self.len], dtype=torch.int64, device=dev)
+        # zero-filled so that the warm-up canvas run by capture() reads finite values
+        self.q = torch.zeros((steps, C, Hq, self.hd), dtype=dt, device=dev)
+        self.kc = torch.zeros((steps + 1, self.Hkv, C, self.hd), dtype=dt, device=dev)  # [steps] = appended K
+        self.vc = torch.zeros_like(self.kc)
+        self.h = torch.zeros((steps, C, self.d), dtype=dt, device=dev)
+        self.tokens = torch.empty(C, dtype=torch.int32, device=dev)
+        self.out = StepOutputs(
+            attn_out=torch.empty((C, Hq, self.hd), dtype=dt, device=dev),
+            attn_lse=torch.empty((Hq, C), dtype=torch.float32, device=dev),
+            argmax=torch.empty(C, dtype=torch.int32, device=dev),
+            conf=torch.empty(C, dtype=torch.float32, device=dev),
+            lse=torch.empty(C, dtype=torch.float32, device=dev),
+            selfcond=torch.empty((C, self.d), dtype=dt, device=dev),
+            renoised=torch.empty(C, dtype=torch.uint8, device=dev))
+        wa = B.canvas_attn_workspace_size(C, Hq, self.Hkv, self.hd, self.prefix_max, B.DG_BF16)
+        self.ws_attn = torch.empty(max(wa, 256), dtype=torch.uint8, device=dev)
+        self.ws_vocab = torch.empty(max(B.vocab_step_workspace_size(C, self.V, self.d), 256), dtype=torch.uint8,
+                                    device=dev)
+        self.graph = None
+
+    def _canvas(self):
+        o, s_ = self.out, self.stream
+        B.canvas_init_devpos(self.tokens, self.V, self.seed, self.len_dev, stream=s_)
+        for s in range(self.steps):
+            B.canvas_attn_devlen(self.q[s], self.k_cache, self.v_cache, self.len_dev, self.prefix_max, self.kc[s],
+                                 self.vc[s], out=o.attn_out, lse=o.attn_lse, workspace=self.ws_attn, stream=s_)
+            B.vocab_step_renoise_devpos(self.h[s], self.emb, self.tokens, self.threshold, self.seed, s, self.len_dev,
+                                        o.argmax, o.conf, o.lse, o.selfcond, o.renoised, self.ws_vocab, stream=s_)
+        B.kv_append_devlen(self.k_cache, self.v_cache, self.len_dev, self.kc[self.steps], self.vc[self.steps],
+                           stream=s_)
+
+    def capture(self):
+        """Records one canvas as a CUDA graph (after one eager warm-up canvas,
+        which the caller's first `run_block` replaces: the length is restored)."""
+        saved = self.len_dev.clone()
+        k0, v0 = self.k_cache.clone(), self.v_cache.clone()
+        with torch.cuda.stream(self.stream):
+            self._canvas()  # warm-up: kernel attributes and tensor maps set outside capture
+        self.stream.synchronize()
+        self.len_dev.copy_(saved)
+        self.k_cache.copy_(k0)
+        self.v_cache.copy_(v0)
+        torch.cuda.synchronize()
+        self.graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.graph, stream=self.stream):
+            self._canvas()
+        return self.graph
+
+    def load_block(self, q, kc, vc, h):
+        """Per-step backbone tensors of the next block: q/kc/vc/h stacked over
+        steps; kc/vc carry one more entry, the finished canvas's K/V."""
+        with torch.cuda.stream(self.stream):
+            self.q.copy_(q, non_blocking=True)
+            self.kc.copy_(kc, non_blocking=True)
+            self.vc.copy_(vc, non_blocking=True)
+            self.h.copy_(h, non_blocking=True)
+
+    def run_block(self):
+        """One canvas: a graph replay; returns its final tokens (device)."""
+        with torch.cuda.stream(self.stream):
+            self.graph.replay()
+        self.len += self.C
+        return self.tokens

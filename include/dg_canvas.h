@@ -233,6 +233,43 @@ DG_API int dg_canvas_fill(int32_t* tokens, int C, int32_t value, void* stream);
  * stop: a step whose renoised flags are all zero finishes the canvas). */
 DG_API int dg_count_flags(const uint8_t* flags, int C, int32_t* count, void* stream);
 
+/* ---------------------------------------------------------------- device-side cache length
+ * Block diffusion (DiffusionGemma explainer, "Multi-canvas sampling (block
+ * diffusion)") appends every finished canvas to the cache, so the prefix
+ * grows by C per canvas. These variants read the prefix length / position
+ * offset from device memory instead of a host argument, so one captured CUDA
+ * graph of a canvas (init, steps, append) can be replayed for every block.
+ * Results are those of the host-length calls with the same values.
+ *
+ * dg_canvas_attn_devlen: dg_canvas_attn with P = *prefix_len_dev, which must
+ * lie in [0, prefix_max] (prefix_max <= cap; outside: clamped, and
+ * DG_ERR_DEVICE_BOUNDS latched). The kernel is planned for prefix_max, so the
+ * workspace is dg_canvas_attn_workspace_size(C, Hq, Hkv, hd, prefix_max, dtype).
+ * Cache rows [P, prefix_max) are read and masked out: they must hold finite
+ * values (zero-initialise the cache once). DG_BF16 and hd == 128 only.
+ */
+DG_API int dg_canvas_attn_devlen(const void* q, const void* k_cache, const void* v_cache, int64_t cap,
+                                 const int64_t* prefix_len_dev, int64_t prefix_max, const void* k_canvas,
+                                 const void* v_canvas, void* out, float* lse, int C, int Hq, int Hkv, int hd,
+                                 float scale, int dtype, int mask, void* workspace, size_t workspace_bytes,
+                                 void* stream);
+
+/* dg_canvas_init with abs_pos0 = *abs_pos0_dev. */
+DG_API int dg_canvas_init_devpos(int32_t* tokens, int C, int V, uint64_t seed, const int64_t* abs_pos0_dev,
+                                 void* stream);
+
+/* dg_vocab_step_renoise with abs_pos0 = *abs_pos0_dev (DG_BF16 only). */
+DG_API int dg_vocab_step_renoise_devpos(const void* h, const void* emb, int C, int V, int d, int dtype,
+                                        int32_t* argmax, float* conf, float* lse, void* selfcond, int32_t* tokens,
+                                        float threshold, uint64_t seed, uint32_t step, const int64_t* abs_pos0_dev,
+                                        uint8_t* renoised, void* workspace, size_t workspace_bytes, void* stream);
+
+/* dg_kv_append without the attention, at P = *len_dev on the device, then
+ * *len_dev += C on the device. If P < 0 or P + C > cap nothing is written,
+ * *len_dev is unchanged and DG_ERR_DEVICE_BOUNDS is latched. */
+DG_API int dg_kv_append_devlen(void* k_cache, void* v_cache, int64_t cap, int64_t* len_dev, const void* k_new,
+                               const void* v_new, int C, int Hkv, int hd, int dtype, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -130,3 +130,54 @@ def test_early_stop_and_next_input(lib):
 
     generate(den, 2, 3, backbone, on_step=on_step, early_stop=True)
     assert den.steps_taken == [1, 3]
+
+
+def test_graphed_block_diffusion_matches_eager(lib):
+    """One CUDA graph per canvas with the cache length on the device, replayed
+    for every block, gives the eager host-length run's tokens and cache
+    bytes, and attention within tolerance of the oracle."""
+    from canvas_denoising_gb300.driver import GraphedBlockDiffusion
+    C, V, d, Hq, Hkv, hd, P0, blocks, steps = 256, 8192, 256, 16, 8, 128, 512, 3, 3
+    thr, seed, alpha = 0.3, 21, 6.0
+    emb = synth.embedding(V, d, seed, std=0.1)
+    cap = P0 + blocks * C
+    k, v = synth.kv_prefix(Hkv, cap, hd, P0, seed)
+    k[:, P0:] = 0  # rows past the prefix: finite (the device-length attention reads and masks them)
+    v[:, P0:] = 0
+
+    def inputs(b, s):
+        q, kc, vc = synth.canvas_qkv(C, Hq, Hkv, hd, seed, block=b, step=s)
+        h = synth.hidden(emb, synth.targets(C, V, seed, block=b), alpha, seed, block=b, step=s)
+        return q, kc, vc, h
+
+    # eager, host length
+    ke, ve = k.cuda(), v.cuda()
+    den = CanvasDenoiser(emb.cuda(), ke, ve, P0, C, Hq, thr, seed)
+
+    def backbone(b, s, tokens, selfcond):
+        return tuple(x.cuda() for x in inputs(b, s))
+
+    eager = [t.cpu() for t in generate(den, blocks, steps, backbone)]
+    # graphed, device length
+    kg, vg = k.cuda(), v.cuda()
+    stream = torch.cuda.Stream()
+    gb = GraphedBlockDiffusion(emb.cuda(), kg, vg, P0, C, Hq, thr, seed, steps, stream)
+    gb.capture()
+    for b in range(blocks):
+        per = [inputs(b, s) for s in range(steps + 1)]
+        gb.load_block(torch.stack([p[0] for p in per[:steps]]).cuda(), torch.stack([p[1] for p in per]).cuda(),
+                      torch.stack([p[2] for p in per]).cuda(), torch.stack([p[3] for p in per[:steps]]).cuda())
+        tok = gb.run_block()
+        stream.synchronize()
+        np.testing.assert_array_equal(_np(tok), eager[b].numpy(), err_msg=f"block {b}")
+        # the last step's attention, against the oracle over the cache as it stood
+        q, kc, vc, _ = per[steps - 1]
+        P = P0 + b * C
+        ro, rl = oracle.canvas_attention(_np(q), _np(kg.cpu())[:, :P], _np(vg.cpu())[:, :P], P, _np(kc), _np(vc))
+        assert_rows_close(_np(gb.out.attn_out).reshape(-1, hd), ro.reshape(-1, hd), what=f"graphed attn b{b}")
+        assert np.abs(_np(gb.out.attn_lse) - rl).max() <= LSE_ABS
+    assert int(gb.len_dev.item()) == P0 + blocks * C == den.len
+    np.testing.assert_array_equal(_np(kg), _np(ke))
+    np.testing.assert_array_equal(_np(vg), _np(ve))
+    from canvas_denoising_gb300 import binding as B
+    assert B.device_status() == B.DG_OK

@@ -118,7 +118,7 @@ def test_canvas_fill_and_count(lib):
 
 
 # ------------------------------------------------------------------ prompt prefill shapes
-@pytest.mark.parametrize("P,C", [(0, 2048), (1024, 2048), (0, 520)])
+@pytest.mark.parametrize("P,C", [(0, 2048), (1024, 2048), (0, 520), (0, 4096)])
 def test_prefill_shapes_causal_append(lib, P, C):
     """Incremental causal prefill of a whole prompt chunk (the step before the
     denoising loop): a C-row block appended at P, with its causal attention."""
