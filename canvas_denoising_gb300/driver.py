@@ -150,7 +150,7 @@ class GraphedBlockDiffusion:
     diffusion)"). The backbone's per-step tensors are read from fixed buffers,
     which the caller fills before each replay (`load_block`)."""
 
-    def __init__(self, emb, k_cache, v_cache, prefix_len, C, Hq, threshold, seed, steps, stream):
+    def __init__(self, emb, k_cache, v_cache, prefix_len, C, Hq, threshold, seed, steps, stream, events=None):
         self.emb, self.k_cache, self.v_cache = emb, k_cache, v_cache
         self.Hkv, self.cap, self.hd = k_cache.shape
         self.V, self.d = emb.shape
@@ -179,15 +179,24 @@ class GraphedBlockDiffusion:
         self.ws_vocab = torch.empty(max(B.vocab_step_workspace_size(C, self.V, self.d), 256), dtype=torch.uint8,
                                     device=dev)
         self.graph = None
+        self.events = events  # optional per-step (attn start, attn end, vocab start, vocab end) timing events
+        self.launches = 1 + 3 * steps + 2  # kernels per canvas: init, steps x (attention + vocab 2), append 2
 
     def _canvas(self):
-        o, s_ = self.out, self.stream
+        o, s_, ev = self.out, self.stream, self.events
         B.canvas_init_devpos(self.tokens, self.V, self.seed, self.len_dev, stream=s_)
         for s in range(self.steps):
+            if ev is not None:
+                ev[s][0].record(s_)
             B.canvas_attn_devlen(self.q[s], self.k_cache, self.v_cache, self.len_dev, self.prefix_max, self.kc[s],
                                  self.vc[s], out=o.attn_out, lse=o.attn_lse, workspace=self.ws_attn, stream=s_)
+            if ev is not None:
+                ev[s][1].record(s_)
+                ev[s][2].record(s_)
             B.vocab_step_renoise_devpos(self.h[s], self.emb, self.tokens, self.threshold, self.seed, s, self.len_dev,
                                         o.argmax, o.conf, o.lse, o.selfcond, o.renoised, self.ws_vocab, stream=s_)
+            if ev is not None:
+                ev[s][3].record(s_)
         B.kv_append_devlen(self.k_cache, self.v_cache, self.len_dev, self.kc[self.steps], self.vc[self.steps],
                            stream=s_)
 
@@ -196,8 +205,10 @@ class GraphedBlockDiffusion:
         which the caller's first `run_block` replaces: the length is restored)."""
         saved = self.len_dev.clone()
         k0, v0 = self.k_cache.clone(), self.v_cache.clone()
+        ev, self.events = self.events, None
         with torch.cuda.stream(self.stream):
             self._canvas()  # warm-up: kernel attributes and tensor maps set outside capture
+        self.events = ev
         self.stream.synchronize()
         self.len_dev.copy_(saved)
         self.k_cache.copy_(k0)
