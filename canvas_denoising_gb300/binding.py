@@ -54,6 +54,7 @@ _SIGS = {
     "dg_vocab_step_renoise_devpos": (_c_int, [_p, _p, _c_int, _c_int, _c_int, _c_int, _p, _p, _p, _p, _p, _c_f,
                                               _c_u64, _c_u32, _p, _p, _p, _c_sz, _p]),
     "dg_kv_append_devlen": (_c_int, [_p, _p, _c_i64, _p, _p, _p, _c_int, _c_int, _c_int, _c_int, _p]),
+    "dg_debug_inject": (_c_int, [_c_int, _c_int]),
 }
 
 EXPORTS = tuple(_SIGS)
@@ -385,3 +386,13 @@ def kv_append_devlen(k_cache, v_cache, len_dev, k_new, v_new, stream=None):
     rc = load().dg_kv_append_devlen(_ptr(k_cache), _ptr(v_cache), cap, _ptr(len_dev), _ptr(k_new), _ptr(v_new),
                                     k_new.shape[1], Hkv, hd, _dtype_code(k_cache), _stream(stream))
     _check("dg_kv_append_devlen", rc)
+
+
+# ------------------------------------------------------------------ failure injection (tests)
+INJECT_NONE, INJECT_ATTN_ARRIVAL, INJECT_VOCAB_READY = 0, 1, 2
+
+
+def debug_inject(kind: int, wait_ms: int = 0):
+    """The next launch of the named kernel withholds one cross-CTA arrival, so
+    its bounded waits expire (DG_ERR_TIMEOUT) after `wait_ms`."""
+    _check("dg_debug_inject", load().dg_debug_inject(int(kind), int(wait_ms)))

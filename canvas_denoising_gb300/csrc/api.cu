@@ -26,6 +26,21 @@ int* status_ptr() {
   return addr[dev];
 }
 
+namespace {
+std::mutex g_inject_mu;
+Inject g_inject{kInjectNone, 0};
+}  // namespace
+
+Inject take_inject(int kind) {
+  std::lock_guard<std::mutex> lk(g_inject_mu);
+  Inject r{kInjectNone, 0};
+  if (g_inject.kind == kind) {
+    r = g_inject;
+    g_inject = Inject{kInjectNone, 0};
+  }
+  return r;
+}
+
 void report_cuda_error(cudaError_t e, const char* what, const char* file, int line) {
   static const bool verbose = [] {
     const char* v = getenv("DG_VERBOSE");
@@ -171,4 +186,18 @@ extern "C" int dg_canvas_attn_devlen(const void* q, const void* k_cache, const v
   if (scale <= 0.f) scale = 1.0f / sqrtf((float)hd);
   return attn_tc_launch(q, k_cache, v_cache, cap, prefix_max, k_canvas, v_canvas, out, lse, C, Hq, Hkv, scale, mask,
                         workspace, workspace_bytes, (cudaStream_t)stream, prefix_len_dev);
+}
+
+extern "C" int dg_debug_inject(int kind, int wait_ms) {
+  if (kind < kInjectNone || kind > kInjectVocabReady || wait_ms < 0 || wait_ms > 10000) return DG_ERR_INVALID_ARG;
+  long long cycles = 0;
+  if (kind != kInjectNone) {
+    int dev = 0, khz = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&khz, cudaDevAttrClockRate, dev) != cudaSuccess)
+      return DG_ERR_CUDA;
+    cycles = (long long)wait_ms * khz;  // kHz x ms = cycles
+  }
+  std::lock_guard<std::mutex> lk(g_inject_mu);
+  g_inject = Inject{kind, cycles};
+  return DG_OK;
 }

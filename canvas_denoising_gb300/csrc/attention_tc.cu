@@ -81,12 +81,15 @@ struct TcArgs {
   float scale_log2;
   int causal;
   int q_tma;  // Q tiles by TMA (the stacked rows of 128 / group positions form one box)
+  int inject;  // test injection: split 0 withholds its arrival on the merge counter
+  long long wait_cycles;
   int* status;
 };
 
 struct Ctl {
   volatile int* abort;
   int* status;
+  long long wait_cycles;
 };
 
 __device__ bool wait_bar(uint32_t bar, uint32_t parity, const Ctl& c) {
@@ -96,11 +99,25 @@ __device__ bool wait_bar(uint32_t bar, uint32_t parity, const Ctl& c) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((it & 255u) == 0) {
       if (*c.abort) return false;
-      if (clock64() - t0 > kTimeoutCycles) {
+      if (clock64() - t0 > c.wait_cycles) {
         *c.abort = 1;
         latch(c.status, DG_ERR_TIMEOUT);
         return false;
       }
+    }
+  }
+}
+
+// Drain wait for this CTA's own TMA copies / MMAs before TMEM is freed: bounded
+// by time only, not cut short by the abort flag.
+__device__ void drain_bar(uint32_t bar, uint32_t parity, const Ctl& c) {
+  const long long t0 = clock64();
+  for (uint32_t it = 0;; ++it) {
+    if (mbar_try_wait(bar, parity)) return;
+    if ((it & 255u) == 0 && clock64() - t0 > c.wait_cycles) {
+      *c.abort = 1;
+      latch(c.status, DG_ERR_TIMEOUT);
+      return;
     }
   }
 }
@@ -152,7 +169,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t sbase = smem_addr(sm);
   const int mblk = blockIdx.x, g = blockIdx.y, split = blockIdx.z;
   const int64_t M = (int64_t)a.grp * a.C;
-  Ctl ctl{&abort_flag, a.status};
+  Ctl ctl{&abort_flag, a.status, a.wait_cycles};
 
   // key range: the cache prefix P (from device memory when P_dev is set; the
   // tensor maps then span P_max rows, and rows past P are masked below)
@@ -261,7 +278,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         par[slot] = ph;
       }
       for (int s = 0; s < kRing; ++s)
-        if (issued[s]) wait_bar(smem_addr(&ring_full[s]), par[s], ctl);
+        if (issued[s]) drain_bar(smem_addr(&ring_full[s]), par[s], ctl);
     }
     __syncwarp();
   } else if (warp == 1) {
@@ -329,7 +346,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       mma_commit(smem_addr(&drain));
-      wait_bar(smem_addr(&drain), 0, ctl);
+      drain_bar(smem_addr(&drain), 0, ctl);
     }
     __syncwarp();
   } else {
@@ -499,11 +516,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (tid == 0) {
       bulk_wait_all();
       fence_proxy_async_global();  // the bulk-copied rows, before the release below
-      red_release_add_gpu(a.arrived + grp_id, 1);
+      if (!(a.inject && split == 0)) red_release_add_gpu(a.arrived + grp_id, 1);
       bool go = true;
       const long long t0 = clock64();
       while ((int)ld_acquire_gpu(a.arrived + grp_id) < cs) {
-        if (abort_flag || clock64() - t0 > kTimeoutCycles) {
+        if (abort_flag || clock64() - t0 > a.wait_cycles) {
           latch(a.status, DG_ERR_TIMEOUT);
           go = false;
           break;
@@ -733,6 +750,9 @@ int attn_tc_launch(const void* q, const void* k_cache, const void* v_cache, int6
   a.scale_log2 = scale * 1.4426950408889634f;
   a.causal = mask == DG_MASK_CAUSAL_BLOCK;
   a.q_tma = q_tma;
+  const Inject inj = take_inject(kInjectAttnArrival);
+  a.inject = inj.kind != kInjectNone && splits > 1;
+  a.wait_cycles = inj.wait_cycles > 0 ? inj.wait_cycles : kTimeoutCycles;
   a.status = st;
   const int64_t M = (int64_t)a.grp * C;
   cudaLaunchConfig_t cfg = {};

@@ -166,6 +166,8 @@ struct Params {
   uint32_t rn_step;
   int64_t rn_pos0;
   const int64_t* rn_pos0_dev;  // device-side position offset (or null)
+  int inject;                  // test injection: tile 0's ready flag is never released
+  long long wait_cycles;       // bound of every wait
   int* status;
 };
 
@@ -184,10 +186,25 @@ __device__ bool wait_bar(uint32_t bar, uint32_t parity, const Params& p) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((it & 255u) == 0) {
       if (aborted(p.abort_flag)) return false;
-      if (clock64() - t0 > kTimeoutCycles) {
+      if (clock64() - t0 > p.wait_cycles) {
         raise_abort(p);
         return false;
       }
+    }
+  }
+}
+
+// Drain wait for this CTA's own TMA copies / MMAs before it frees TMEM or
+// exits: bounded by time only (not cut short by an abort, so nothing of this
+// CTA is in flight when it leaves); copies and MMAs already issued complete
+// on their own.
+__device__ void drain_bar(uint32_t bar, uint32_t parity, const Params& p) {
+  const long long t0 = clock64();
+  for (uint32_t it = 0;; ++it) {
+    if (mbar_try_wait(bar, parity)) return;
+    if ((it & 255u) == 0 && clock64() - t0 > p.wait_cycles) {
+      raise_abort(p);
+      return;
     }
   }
 }
@@ -198,7 +215,7 @@ __device__ bool wait_flag(const int* flag, int target, const Params& p) {
   for (uint32_t it = 0;; ++it) {
     if ((int)ld_acquire_gpu(flag) >= target) return true;
     if (aborted(p.abort_flag)) return false;
-    if (clock64() - t0 > kTimeoutCycles) {
+    if (clock64() - t0 > p.wait_cycles) {
       raise_abort(p);
       return false;
     }
@@ -298,7 +315,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         for (int s = 0; s < kStages; ++s)
-          if (issued[s]) wait_bar(smem_addr(&bar_full[s]), issued_par[s], p);
+          if (issued[s]) drain_bar(smem_addr(&bar_full[s]), issued_par[s], p);
       }
       __syncwarp();
     } else if (warp == 1) {
@@ -329,7 +346,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (ok) mma_commit(smem_addr(&bar_tfull));
         }
         mma_commit(smem_addr(&bar_drain));
-        wait_bar(smem_addr(&bar_drain), 0, p);
+        drain_bar(smem_addr(&bar_drain), 0, p);
       }
       __syncwarp();
     } else {
@@ -440,7 +457,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         fence_proxy_async_global();
         __threadfence();
         epi_sync();
-        if (threadIdx.x == 64) red_release_add_gpu(p.ready + t, 1);
+        if (threadIdx.x == 64 && !(p.inject && t == 0)) red_release_add_gpu(p.ready + t, 1);
       }
       if (active && i < p.C) {
         p.am[(size_t)i * p.n_a + a] = m_run;
@@ -495,7 +512,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (ok) atomicAdd(p.consumed + t, 1);
         }
         for (int s = 0; s < kStages; ++s)
-          if (issued[s]) wait_bar(smem_addr(&bar_full[s]), issued_par[s], p);
+          if (issued[s]) drain_bar(smem_addr(&bar_full[s]), issued_par[s], p);
       }
       __syncwarp();
     } else if (warp == 1) {
@@ -523,7 +540,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         mma_commit(smem_addr(&bar_tfull));
-        wait_bar(smem_addr(&bar_tfull), 0, p);
+        drain_bar(smem_addr(&bar_tfull), 0, p);
       }
       __syncwarp();
     } else {
@@ -778,6 +795,9 @@ int vocab_tc_launch(const __nv_bfloat16* h, const __nv_bfloat16* emb, int C, int
   p.rn_step = rn ? rn->step : 0;
   p.rn_pos0 = rn ? rn->abs_pos0 : 0;
   p.rn_pos0_dev = rn ? rn->abs_pos0_dev : nullptr;
+  const Inject inj = take_inject(kInjectVocabReady);
+  p.inject = inj.kind != kInjectNone;
+  p.wait_cycles = inj.wait_cycles > 0 ? inj.wait_cycles : kTimeoutCycles;
   DG_CUDA_TRY(cudaMemsetAsync(flags, 0, L.flag_bytes, s));
 
   const size_t smem = (size_t)kStages * kStageBytes + 1024;

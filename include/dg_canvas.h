@@ -270,6 +270,23 @@ DG_API int dg_vocab_step_renoise_devpos(const void* h, const void* emb, int C, i
 DG_API int dg_kv_append_devlen(void* k_cache, void* v_cache, int64_t cap, int64_t* len_dev, const void* k_new,
                                const void* v_new, int C, int Hkv, int hd, int dtype, void* stream);
 
+/* ---------------------------------------------------------------- failure injection (tests)
+ * Not part of the method (the explainer pages have no counterpart): a test
+ * hook that makes the NEXT launch of one kernel fail its cross-CTA handshake
+ * without any fault, so that the bounded waits, DG_ERR_TIMEOUT and the
+ * recovery of the context can be exercised on a GPU.
+ *   kind 0: clear a pending injection
+ *   kind 1: dg_canvas_attn (head_dim 128, more than one key split): key split
+ *           0 of every group withholds its arrival on the merge counter
+ *   kind 2: dg_vocab_step / dg_vocab_step_renoise (bf16): the P tile 0 ready
+ *           flag is never released
+ * wait_ms bounds every wait of that launch (0: the default, about 2 s; at
+ * most 10000). The launch then latches DG_ERR_TIMEOUT in the device status
+ * word, its outputs are undefined, and every CTA returns; later launches run
+ * normally. Host-side state, one pending injection per process.
+ */
+DG_API int dg_debug_inject(int kind, int wait_ms);
+
 #ifdef __cplusplus
 }
 #endif

@@ -108,3 +108,10 @@ def test_vocab_plan_is_a_host_query(lib):
     n_a, n_c, ks, pair, grid, n_vt = list(buf)
     assert n_vt == 1024 and n_c % 11 == 0 and n_c // 11 == ks and n_a + n_c <= grid <= n_a + n_c + 1
     assert lib.dg_vocab_step_plan(256, 262144, 2800, B.DG_BF16, ctypes.cast(buf, ctypes.c_void_p)) == B.DG_ERR_INVALID_ARG
+
+
+def test_debug_inject_validates(lib):
+    assert lib.dg_debug_inject(7, 0) == B.DG_ERR_INVALID_ARG
+    assert lib.dg_debug_inject(1, -1) == B.DG_ERR_INVALID_ARG
+    assert lib.dg_debug_inject(1, 20000) == B.DG_ERR_INVALID_ARG
+    assert lib.dg_debug_inject(0, 0) == B.DG_OK  # clearing needs no device
