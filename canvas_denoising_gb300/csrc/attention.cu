@@ -382,24 +382,29 @@ template <typename OutT>
 __global__ void __launch_bounds__(256) attn_combine(const float* __restrict__ part_o,
                                                     const float* __restrict__ part_lse, OutT* out, float* lse, int C,
                                                     int Hq, int HD, int splits) {
+  // one warp per (position, head); split weights in shared memory (lanes
+  // hold splits s = lane and lane + 32)
+  __shared__ float s_w[256 / 32][kMaxSplits];
+  const int wib = threadIdx.x >> 5;
   const int64_t w = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   if (w >= (int64_t)C * Hq) return;
   const int64_t i = w / Hq, h = w % Hq;
-  float lw[kMaxSplits];
-  float mx = -INFINITY;
-#pragma unroll 8
-  for (int s = 0; s < splits; ++s) {
-    lw[s] = __ldg(part_lse + ((int64_t)s * Hq + h) * C + i);
-    mx = fmaxf(mx, lw[s]);
-  }
+  float x0 = -INFINITY, x1 = -INFINITY;
+  if (lane < splits) x0 = __ldg(part_lse + ((int64_t)lane * Hq + h) * C + i);
+  if (lane + 32 < splits) x1 = __ldg(part_lse + ((int64_t)(lane + 32) * Hq + h) * C + i);
+  float mx = fmaxf(x0, x1);
+#pragma unroll
+  for (int o = 16; o; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
   const float ref = mx == -INFINITY ? 0.f : mx;
-  float tot = 0.f;
-#pragma unroll 8
-  for (int s = 0; s < splits; ++s) {
-    lw[s] = __expf(lw[s] - ref);
-    tot += lw[s];
-  }
+  const float e0 = lane < splits ? __expf(x0 - ref) : 0.f;
+  const float e1 = lane + 32 < splits ? __expf(x1 - ref) : 0.f;
+  float tot = e0 + e1;
+#pragma unroll
+  for (int o = 16; o; o >>= 1) tot += __shfl_xor_sync(0xffffffffu, tot, o);
+  s_w[wib][lane] = e0;
+  s_w[wib][lane + 32] = e1;
+  __syncwarp();
   const float inv = tot > 0.f ? 1.f / tot : 0.f;
   const float* base = part_o + (i * Hq + h) * HD;
   const int64_t sstride = (int64_t)C * Hq * HD;
@@ -407,11 +412,12 @@ __global__ void __launch_bounds__(256) attn_combine(const float* __restrict__ pa
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll 8
     for (int s = 0; s < splits; ++s) {
+      const float ws = s_w[wib][s];
       const float4 v = __ldg(reinterpret_cast<const float4*>(base + s * sstride + c));
-      acc.x = fmaf(lw[s], v.x, acc.x);
-      acc.y = fmaf(lw[s], v.y, acc.y);
-      acc.z = fmaf(lw[s], v.z, acc.z);
-      acc.w = fmaf(lw[s], v.w, acc.w);
+      acc.x = fmaf(ws, v.x, acc.x);
+      acc.y = fmaf(ws, v.y, acc.y);
+      acc.z = fmaf(ws, v.z, acc.z);
+      acc.w = fmaf(ws, v.w, acc.w);
     }
     OutT* o = out + (i * Hq + h) * HD + c;
     o[0] = (OutT)(acc.x * inv);

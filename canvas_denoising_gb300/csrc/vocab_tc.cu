@@ -62,7 +62,6 @@ constexpr uint32_t kTileBytes = 16384u;  // [128 rows x 64 bf16], one swizzled o
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kTau = 40.f;       // overflow margin above the reference, natural log
 constexpr long long kTimeoutCycles = 4000000000ll;
-constexpr int kPrefetch = 0;       // producer k-steps of E prefetched into L2 ahead (measured: 12 was slower)
 
 struct Plan {
   int n_rh, n_dt, n_vt, ksplit, n_a, n_c, window;
