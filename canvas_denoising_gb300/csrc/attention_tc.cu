@@ -391,10 +391,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         float m8[8];
 #pragma unroll
-        for (int e = 0; e < 8; ++e) m8[e] = v[e];
+        for (int e = 0; e < 8; ++e) m8[e] = fmaxf(v[e], v[120 + e]);
 #pragma unroll
-        for (int e = 8; e < kBN; ++e) m8[e & 7] = fmaxf(m8[e & 7], v[e]);
-        mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])), fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
+        for (int b = 8; b < 120; b += 16)
+#pragma unroll
+          for (int e = 0; e < 8; ++e) m8[e] = max3(m8[e], v[b + e], v[b + 8 + e]);
+        mx = max3(max3(m8[0], m8[1], m8[2]), max3(m8[3], m8[4], m8[5]), fmaxf(m8[6], m8[7]));
       }
       const float mt = mx * a.scale_log2;  // scale > 0 keeps the order
       bool need = false;
@@ -410,34 +412,36 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       const float rr = ref == -INFINITY ? 0.f : ref;
-      uint32_t pk[kBN / 2];
+      // P over the first 64 columns of S_q, 32 columns (two S chunks) at a time:
+      // P columns [32h, 32h + 32) hold S elements already read (chunk h).
       float sum8[8];
 #pragma unroll
       for (int e = 0; e < 8; ++e) sum8[e] = 0.f;
+      const float sl2 = a.scale_log2, nrr = -rr;
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        float s32[32];
-        tmem_ld32(tS + loff + c * 32, s32);
-        if (lim < (c + 1) * 32) {
+      for (int hf = 0; hf < 2; ++hf) {
+        uint32_t pk[32];
 #pragma unroll
-          for (int e = 0; e < 32; ++e)
-            if (c * 32 + e >= lim) s32[e] = -INFINITY;
-        }
+        for (int cc = 0; cc < 2; ++cc) {
+          const int c = hf * 2 + cc;
+          float s32[32];
+          tmem_ld32(tS + loff + c * 32, s32);
+          if (lim < (c + 1) * 32) {
 #pragma unroll
-        for (int g8 = 0; g8 < 4; ++g8) {
-          float p8[8];
-#pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            p8[e] = ex2_approx(fmaf(s32[g8 * 8 + e], a.scale_log2, -rr));  // exp2(-inf) = 0 when masked
-            sum8[e] += p8[e];
+            for (int e = 0; e < 32; ++e)
+              if (c * 32 + e >= lim) s32[e] = -INFINITY;
           }
 #pragma unroll
-          for (int e = 0; e < 4; ++e) pk[c * 16 + g8 * 4 + e] = pack2(p8[2 * e], p8[2 * e + 1]);
+          for (int g = 0; g < 16; ++g) {  // element pair (2g, 2g + 1) of the chunk
+            float x0, x1;
+            fma2(x0, x1, s32[2 * g], s32[2 * g + 1], sl2, sl2, nrr, nrr);
+            const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);  // exp2(-inf) = 0 for masked keys
+            add2(sum8[2 * (g & 3)], sum8[2 * (g & 3) + 1], p0, p1);
+            pk[cc * 16 + g] = pack2(p0, p1);
+          }
         }
+        tmem_st32_async(tS + loff + hf * 32, pk);
       }
-      // P over the first 64 columns of S_q (S is no longer needed)
-      tmem_st32_async(tS + loff, pk);
-      tmem_st32_async(tS + loff + 32, pk + 32);
       l += ((sum8[0] + sum8[1]) + (sum8[2] + sum8[3])) + ((sum8[4] + sum8[5]) + (sum8[6] + sum8[7]));
       // O_q holds every PV_q issued so far (complete: covered by this tile's
       // s_full commit); rescale it before PV_q(jj) adds to it.
