@@ -419,11 +419,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           // when the chunk beats the running max (first index attaining it)
           float bm[8];
 #pragma unroll
-          for (int e = 0; e < 8; ++e) bm[e] = v[e];
+          for (int e = 0; e < 8; ++e) bm[e] = fmaxf(v[e], v[120 + e]);
 #pragma unroll
-          for (int e = 8; e < 128; ++e) bm[e & 7] = fmaxf(bm[e & 7], v[e]);
-          const float cm = fmaxf(fmaxf(fmaxf(bm[0], bm[1]), fmaxf(bm[2], bm[3])),
-                                 fmaxf(fmaxf(bm[4], bm[5]), fmaxf(bm[6], bm[7])));
+          for (int b = 8; b < 120; b += 16)
+#pragma unroll
+            for (int e = 0; e < 8; ++e) bm[e] = max3(bm[e], v[b + e], v[b + 8 + e]);
+          const float cm = max3(max3(bm[0], bm[1], bm[2]), max3(bm[3], bm[4], bm[5]), fmaxf(bm[6], bm[7]));
           if (cm > m_run) {
             int ci = 127;
 #pragma unroll
@@ -441,9 +442,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int e8 = 0; e8 < 16; ++e8) {
             float pe[8];
 #pragma unroll
-            for (int f = 0; f < 8; ++f) {
-              pe[f] = ex2_approx(fmaf(v[e8 * 8 + f], kLog2e, -R2));  // masked ids: exp2(-inf) = 0
-              zs[f] += pe[f];
+            for (int f = 0; f < 8; f += 2) {  // paired fp32 instructions: the epilogue is issue-bound
+              float x0, x1;
+              fma2(x0, x1, v[e8 * 8 + f], v[e8 * 8 + f + 1], kLog2e, kLog2e, -R2, -R2);
+              pe[f] = ex2_approx(x0);  // masked ids: exp2(-inf) = 0
+              pe[f + 1] = ex2_approx(x1);
+              add2(zs[f], zs[f + 1], pe[f], pe[f + 1]);
             }
             const int sub = e8 >> 3, piece = e8 & 7;
             uint8_t* dst = prow + (size_t)sub * p.n_rh * kTileBytes + ((piece ^ (r & 7)) << 4);
