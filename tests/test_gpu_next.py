@@ -134,3 +134,44 @@ def test_prefill_shapes_causal_append(lib, P, C):
     assert_rows_close(_np(out).reshape(C * Hq, hd), ro.reshape(C * Hq, hd), what="prefill out")
     assert np.abs(_np(lse) - rl).max() <= LSE_ABS
     assert B.device_status() == B.DG_OK
+
+
+# ------------------------------------------------------------------ device-side cache length
+def test_devlen_attention_matches_host_length(lib):
+    """dg_canvas_attn_devlen at every prefix a growing cache passes through
+    equals the oracle (rows past the prefix hold finite stale data)."""
+    C, Hq, Hkv, hd, Pmax = 256, 16, 8, 128, 2048
+    k, v = synth.kv_prefix(Hkv, Pmax + C, hd, Pmax, seed=41)
+    q, kn, vn = synth.canvas_qkv(C, Hq, Hkv, hd, seed=41)
+    kd, vd = k.cuda(), v.cuda()
+    for P in (0, 512, 1300, Pmax):
+        pdev = torch.tensor([P], dtype=torch.int64, device="cuda")
+        for mask in (B.DG_MASK_BIDIR, B.DG_MASK_CAUSAL_BLOCK):
+            out, lse = B.canvas_attn_devlen(q.cuda(), kd, vd, pdev, Pmax, kn.cuda(), vn.cuda(), mask=mask)
+            ro, rl = oracle.canvas_attention(_np(q), _np(k), _np(v), P, _np(kn), _np(vn),
+                                             causal=mask == B.DG_MASK_CAUSAL_BLOCK)
+            assert_rows_close(_np(out).reshape(C * Hq, hd), ro.reshape(C * Hq, hd), what=f"devlen P={P} m={mask}")
+            assert np.abs(_np(lse) - rl).max() <= LSE_ABS
+    assert B.device_status() == B.DG_OK
+    # a device prefix beyond the planned maximum is clamped and reported
+    pdev = torch.tensor([Pmax + 7], dtype=torch.int64, device="cuda")
+    B.canvas_attn_devlen(q.cuda(), kd, vd, pdev, Pmax, kn.cuda(), vn.cuda())
+    assert B.device_status() == B.DG_ERR_DEVICE_BOUNDS
+
+
+def test_devlen_append_and_bounds(lib):
+    Hkv, hd, C, cap = 4, 128, 64, 200
+    k = torch.zeros((Hkv, cap, hd), dtype=torch.bfloat16, device="cuda")
+    v = torch.zeros_like(k)
+    kn = synth.normal((Hkv, C, hd), seed=42, purpose="k_canvas").cuda()
+    vn = synth.normal((Hkv, C, hd), seed=42, purpose="v_canvas").cuda()
+    ln = torch.tensor([10], dtype=torch.int64, device="cuda")
+    B.kv_append_devlen(k, v, ln, kn, vn)
+    B.kv_append_devlen(k, v, ln, kn, vn)
+    assert int(ln.item()) == 10 + 2 * C
+    assert torch.equal(k[:, 10:10 + C], kn) and torch.equal(v[:, 10 + C:10 + 2 * C], vn)
+    assert B.device_status() == B.DG_OK
+    before = k.clone()
+    B.kv_append_devlen(k, v, ln, kn, vn)  # 138 + 64 > 200: nothing written, length unchanged
+    assert B.device_status() == B.DG_ERR_DEVICE_BOUNDS
+    assert int(ln.item()) == 10 + 2 * C and torch.equal(k, before)
