@@ -382,34 +382,66 @@ def run_ours(args, world, rank, local):
             attn_ms = statistics.mean(e[2].elapsed_time(e[3]) for e in a_evs)
             del ga
 
-    # ---- end to end through the public API: per-step inputs from pinned host memory, result back
+    # ---- end to end through the public API: per-step inputs from pinned host memory, result back.
+    # As a pipelined caller would: the next step's inputs are copied on a second stream into the
+    # other of two device buffers while the current step computes; each step's result (tokens,
+    # self-conditioning vector) is staged on the device and read back on the copy stream.
     e2e = None
     if not args.no_e2e:
         Ke = min(K, 200)
         host_in = [tuple(x.cpu().pin_memory() for x in cv.inputs[i]) for i in range(cv.N_INPUTS)]
-        dev_in = tuple(torch.empty_like(x) for x in cv.inputs[0])
+        dev_in = [tuple(torch.empty_like(x) for x in cv.inputs[0]) for _ in range(2)]
+        stage = [(torch.empty_like(cv.tokens), torch.empty_like(cv.selfcond)) for _ in range(2)]
         host_tok = torch.empty(w.C, dtype=torch.int32).pin_memory()
         host_sc = torch.empty((w.C, w.d), dtype=cv.dt).pin_memory()
         h2d = sum(x.numel() * x.element_size() for x in host_in[0])
         d2h = host_tok.numel() * 4 + host_sc.numel() * host_sc.element_size()
+        cs = torch.cuda.Stream(device=dev)
+        ev = lambda: torch.cuda.Event()
+        in_ready, in_free, out_ready, out_read = ([ev(), ev()] for _ in range(4))
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+
+        def load(step, b):
+            for dst, src in zip(dev_in[b], host_in[step % cv.N_INPUTS]):
+                dst.copy_(src, non_blocking=True)
+            in_ready[b].record(cs)
+
         if world > 1:
             torch.distributed.barrier()
         torch.cuda.synchronize()
-        with torch.cuda.stream(stream):
-            e0.record(stream)
-            for s in range(Ke):
-                for dst, src in zip(dev_in, host_in[s % cv.N_INPUTS]):
-                    dst.copy_(src, non_blocking=True)
-                cv.step(s, stream, inputs=dev_in)
-                host_tok.copy_(cv.tokens, non_blocking=True)
-                host_sc.copy_(cv.selfcond, non_blocking=True)
-            e1.record(stream)
+        e0.record(stream)
+        cs.wait_event(e0)
+        with torch.cuda.stream(cs):
+            load(0, 0)
+        for s in range(Ke):
+            b = s % 2
+            if s + 1 < Ke:
+                with torch.cuda.stream(cs):
+                    if s >= 1:
+                        cs.wait_event(in_free[1 - b])  # step s-1 is done reading that buffer
+                    load(s + 1, 1 - b)
+            with torch.cuda.stream(stream):
+                stream.wait_event(in_ready[b])
+                if s >= 2:
+                    stream.wait_event(out_read[b])  # the staging buffer's previous read-back is done
+                cv.step(s, stream, inputs=dev_in[b])
+                in_free[b].record(stream)
+                stage[b][0].copy_(cv.tokens, non_blocking=True)
+                stage[b][1].copy_(cv.selfcond, non_blocking=True)
+                out_ready[b].record(stream)
+            with torch.cuda.stream(cs):
+                cs.wait_event(out_ready[b])
+                host_tok.copy_(stage[b][0], non_blocking=True)
+                host_sc.copy_(stage[b][1], non_blocking=True)
+                out_read[b].record(cs)
+        stream.wait_stream(cs)
+        e1.record(stream)
         stream.synchronize()
         ems = e0.elapsed_time(e1)
         ems = max_over_ranks(ems, dev)
         e2e = {"value": round(job_rate(world, Ke, ems), 3), "unit": "steps/s", "h2d_bytes_per_step": int(h2d),
-               "d2h_bytes_per_step": int(d2h), "steps": Ke}
+               "d2h_bytes_per_step": int(d2h), "steps": Ke,
+               "pipelining": "inputs double-buffered on a copy stream; results staged on device, read back there"}
 
     if rank != 0:
         if world > 1:
@@ -424,6 +456,10 @@ def run_ours(args, world, rank, local):
             "frac": round(achieved / pk["bf16_tflops"], 4), "traffic": traffic,
             "peak_source": f"{pk['source']} bf16 burst", "algorithmic_flops_per_launch": flops,
             "avg_launch_ms": round(vocab_ms, 4)}
+    if pk.get("bf16_tflops_sustained"):
+        # the timed loop is ~1000 back-to-back steps under the power cap: the sustained peak applies too
+        roof["peak_sustained"] = pk["bf16_tflops_sustained"]
+        roof["frac_sustained"] = round(achieved / pk["bf16_tflops_sustained"], 4)
     # the step's other contraction: canvas attention (one launch), timed in one more untimed canvas
     # replay with events around every attention call (the timed graph brackets only vocab calls)
     aflops = 4.0 * w.C * (w.prefix + w.C) * w.hd * w.Hq
