@@ -95,7 +95,11 @@ def test_kv_append_rejects_overflow_without_touching(lib):
 # ------------------------------------------------------------------ attention
 @pytest.mark.parametrize("mask", [B.DG_MASK_BIDIR, B.DG_MASK_CAUSAL_BLOCK])
 @pytest.mark.parametrize("C,Hq,Hkv,hd,P", [(40, 4, 2, 128, 37), (256, 8, 4, 128, 1024), (16, 2, 1, 32, 32),
-                                           (77, 6, 3, 64, 0), (1, 2, 2, 128, 300), (130, 16, 8, 128, 700)])
+                                           (77, 6, 3, 64, 0), (1, 2, 2, 128, 300), (130, 16, 8, 128, 700),
+                                           (100, 6, 2, 128, 500),    # group 3: Q staged without TMA
+                                           (64, 8, 2, 128, 256),     # group 4
+                                           (50, 16, 2, 128, 300),    # group 8
+                                           (2400, 16, 8, 128, 64)])  # 152 row-block groups: one key split
 def test_canvas_attn_bf16(lib, mask, C, Hq, Hkv, hd, P):
     cap = P + C + 5
     k, v = synth.kv_prefix(Hkv, cap, hd, P, seed=11)
