@@ -11,8 +11,10 @@
 // head-in-group), so a K/V tile feeds all of them. Keys come in tiles of 128:
 // first the cache rows [0, P), then the canvas rows [0, C); tiles never
 // straddle the two, and the tensor maps' row extents are exactly P and C, so
-// rows past the end read as zeros. K and V tiles stream through a 4-slot TMA
-// ring in the order K0 V0 K1 V1 ...
+// rows past the end read as zeros (with the prefix length read from device
+// memory the cache map spans its upper bound and rows past P are masked).
+// Q arrives by TMA (a 4-D map whose box is 128 stacked rows); K and V tiles
+// stream through a 4-slot TMA ring in the order K0 V0 K1 V1 ...
 //
 // Tensor memory (512 columns): S_q / P_q at 128 q, O_q at 256 + 128 q.
 // For each key tile j and query tile q:
@@ -22,7 +24,9 @@
 //                     kept unless a tile's max exceeds it by 2^8 (then O_q and
 //                     the row sum are rescaled in TMEM), then P = exp2(s - ref)
 //                     from a second read in 32-column chunks, packed to bf16
-//                     and written back over the first 64 columns of S_q
+//                     and written back over the first 64 columns of S_q. The
+//                     softmax is bound by instruction issue: paired fp32
+//                     FMA/add (f32x2) and a three-input max keep it short
 //   O_q += P_q V      tcgen05 with A = P_q read from TMEM, V MN-major in smem
 // The MMA warp issues PV_0(j) S_0(j+1) PV_1(j) S_1(j+1): while one softmax
 // group works, the tensor core runs the other group's two products. Keeping P
@@ -30,10 +34,12 @@
 //
 // Split merge (no second kernel; the launch is cooperative, so every CTA is
 // resident): each CTA stages its normalised O rows (bf16) and per-row lse in
-// shared memory, copies them to its slot of the workspace with coalesced
-// stores, and arrives on its (row block, KV head) counter. Once all splits
-// of the group have arrived, CTA k merges rows [k*ceil(256/splits), ...) with
-// weights exp(lse_s - lse) and writes the bf16 output and the final lse.
+// shared memory, copies them to its slot of the workspace with one bulk copy,
+// and arrives on its (row block, KV head) counter. Once all splits of the
+// group have arrived, CTA k merges rows [k*ceil(256/splits), ...) with
+// weights exp(lse_s - lse) and writes the bf16 output and the final lse. With
+// a single split the staged rows are the output: the launch is not
+// cooperative and the rows are copied straight out.
 // Every wait is bounded (about two seconds); on expiry the CTA latches
 // DG_ERR_TIMEOUT, drains what it issued, frees TMEM and returns.
 #include <cudaTypedefs.h>
