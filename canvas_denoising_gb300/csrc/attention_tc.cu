@@ -417,40 +417,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           l *= factor;
         }
       }
-      const float rr = ref == -INFINITY ? 0.f : ref;
-      // P over the first 64 columns of S_q, 32 columns (two S chunks) at a time:
-      // P columns [32h, 32h + 32) hold S elements already read (chunk h).
-      float sum8[8];
-#pragma unroll
-      for (int e = 0; e < 8; ++e) sum8[e] = 0.f;
-      const float sl2 = a.scale_log2, nrr = -rr;
-#pragma unroll
-      for (int hf = 0; hf < 2; ++hf) {
-        uint32_t pk[32];
-#pragma unroll
-        for (int cc = 0; cc < 2; ++cc) {
-          const int c = hf * 2 + cc;
-          float s32[32];
-          tmem_ld32(tS + loff + c * 32, s32);
-          if (lim < (c + 1) * 32) {
-#pragma unroll
-            for (int e = 0; e < 32; ++e)
-              if (c * 32 + e >= lim) s32[e] = -INFINITY;
-          }
-#pragma unroll
-          for (int g = 0; g < 16; ++g) {  // element pair (2g, 2g + 1) of the chunk
-            float x0, x1;
-            fma2(x0, x1, s32[2 * g], s32[2 * g + 1], sl2, sl2, nrr, nrr);
-            const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);  // exp2(-inf) = 0 for masked keys
-            add2(sum8[2 * (g & 3)], sum8[2 * (g & 3) + 1], p0, p1);
-            pk[cc * 16 + g] = pack2(p0, p1);
-          }
-        }
-        tmem_st32_async(tS + loff + hf * 32, pk);
-      }
-      l += ((sum8[0] + sum8[1]) + (sum8[2] + sum8[3])) + ((sum8[4] + sum8[5]) + (sum8[6] + sum8[7]));
       // O_q holds every PV_q issued so far (complete: covered by this tile's
-      // s_full commit); rescale it before PV_q(jj) adds to it.
+      // s_full commit); rescale it before PV_q(jj) adds to it (and before
+      // P is formed, while few registers are live).
       if (__any_sync(0xffffffffu, need)) {
 #pragma unroll 1
         for (int c = 0; c < 4; ++c) {
@@ -461,6 +430,37 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_st32(tO + loff + c * 32, o);
         }
       }
+      const float rr = ref == -INFINITY ? 0.f : ref;
+      // P over the first 64 columns of S_q, 32 columns at a time: P columns
+      // [32h, 32h + 32) overwrite S elements [32h, 32h + 32), already read.
+      float sum8[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) sum8[e] = 0.f;
+      const float sl2 = a.scale_log2, nrr = -rr;
+#pragma unroll
+      for (int hf = 0; hf < 2; ++hf) {  // S columns [64 hf, 64 hf + 64): one load, one wait
+        float s64[64];
+        tmem_ld64(tS + loff + hf * 64, s64);
+        if (lim < (hf + 1) * 64) {
+#pragma unroll
+          for (int e = 0; e < 64; ++e)
+            if (hf * 64 + e >= lim) s64[e] = -INFINITY;
+        }
+#pragma unroll
+        for (int qt = 0; qt < 2; ++qt) {  // 32 elements -> 16 P columns
+          uint32_t pk[16];
+#pragma unroll
+          for (int g = 0; g < 16; ++g) {  // element pair (2g, 2g + 1) of the quarter
+            float x0, x1;
+            fma2(x0, x1, s64[qt * 32 + 2 * g], s64[qt * 32 + 2 * g + 1], sl2, sl2, nrr, nrr);
+            const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);  // exp2(-inf) = 0 for masked keys
+            add2(sum8[2 * (g & 3)], sum8[2 * (g & 3) + 1], p0, p1);
+            pk[g] = pack2(p0, p1);
+          }
+          tmem_st16_async(tS + loff + hf * 32 + qt * 16, pk);
+        }
+      }
+      l += ((sum8[0] + sum8[1]) + (sum8[2] + sum8[3])) + ((sum8[4] + sum8[5]) + (sum8[6] + sum8[7]));
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(smem_addr(&p_full[q]));
