@@ -383,18 +383,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool got = wait_bar(smem_addr(&s_full[q]), (uint32_t)jj & 1u, ctl);
       if (grp_any(q, !got)) { ok = false; break; }
       tc_fence_after();
-      // Two reads of the S row: the whole row for its max (one 128-column
-      // load), then 32-column chunks for P = exp2(s - ref), packed bf16x2 in
-      // registers until the row is done.
+      // The S row is read twice: all 128 columns for the row max (one load),
+      // whose first 64 values then give the first half of P = exp2(s - ref);
+      // the second half is read again (64 columns). P is packed to bf16x2 and
+      // written over the first 64 columns of S_q, 16 at a time: P columns
+      // [32h, 32h + 32) overwrite S elements [32h, 32h + 32), already read.
+      float v[kBN];
+      tmem_ld128(tS + loff, v);
+      if (lim < kBN) {
+#pragma unroll
+        for (int e = 0; e < kBN; ++e)
+          if (e >= lim) v[e] = -INFINITY;
+      }
       float mx;
       {
-        float v[kBN];
-        tmem_ld128(tS + loff, v);
-        if (lim < kBN) {
-#pragma unroll
-          for (int e = 0; e < kBN; ++e)
-            if (e >= lim) v[e] = -INFINITY;
-        }
         float m8[8];
 #pragma unroll
         for (int e = 0; e < 8; ++e) m8[e] = fmaxf(v[e], v[120 + e]);
@@ -418,8 +420,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       // O_q holds every PV_q issued so far (complete: covered by this tile's
-      // s_full commit); rescale it before PV_q(jj) adds to it (and before
-      // P is formed, while few registers are live).
+      // s_full commit); rescale it before PV_q(jj) adds to it.
       if (__any_sync(0xffffffffu, need)) {
 #pragma unroll 1
         for (int c = 0; c < 4; ++c) {
@@ -431,23 +432,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       const float rr = ref == -INFINITY ? 0.f : ref;
-      // P over the first 64 columns of S_q, 32 columns at a time: P columns
-      // [32h, 32h + 32) overwrite S elements [32h, 32h + 32), already read.
       float sum8[8];
 #pragma unroll
       for (int e = 0; e < 8; ++e) sum8[e] = 0.f;
       const float sl2 = a.scale_log2, nrr = -rr;
+      auto p_half = [&](const float* s64, int hf) {  // 64 S values -> 32 P columns
 #pragma unroll
-      for (int hf = 0; hf < 2; ++hf) {  // S columns [64 hf, 64 hf + 64): one load, one wait
-        float s64[64];
-        tmem_ld64(tS + loff + hf * 64, s64);
-        if (lim < (hf + 1) * 64) {
-#pragma unroll
-          for (int e = 0; e < 64; ++e)
-            if (hf * 64 + e >= lim) s64[e] = -INFINITY;
-        }
-#pragma unroll
-        for (int qt = 0; qt < 2; ++qt) {  // 32 elements -> 16 P columns
+        for (int qt = 0; qt < 2; ++qt) {
           uint32_t pk[16];
 #pragma unroll
           for (int g = 0; g < 16; ++g) {  // element pair (2g, 2g + 1) of the quarter
@@ -459,6 +450,17 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           tmem_st16_async(tS + loff + hf * 32 + qt * 16, pk);
         }
+      };
+      p_half(v, 0);
+      {
+        float s64[64];
+        tmem_ld64(tS + loff + 64, s64);
+        if (lim < kBN) {
+#pragma unroll
+          for (int e = 0; e < 64; ++e)
+            if (64 + e >= lim) s64[e] = -INFINITY;
+        }
+        p_half(s64, 1);
       }
       l += ((sum8[0] + sum8[1]) + (sum8[2] + sum8[3])) + ((sum8[4] + sum8[5]) + (sum8[6] + sum8[7]));
       tmem_wait_st();
