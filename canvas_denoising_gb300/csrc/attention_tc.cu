@@ -468,9 +468,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_arrive(smem_addr(&p_full[q]));
       done_tiles = jj + 1;
     }
-    // epilogue: stage O_q / l (bf16) and the row's lse for the split merge.
-    // The staged rows (64 KB) overwrite the Q tiles: every S product is
-    // complete once o_full[0] fires.
+    // epilogue: O_q / l in bf16 and the row's lse. Several splits: written
+    // straight to this split's slot of the workspace, piece-major ([16-byte
+    // piece][row], so each warp store is 512 contiguous bytes). One split:
+    // staged over the dead Q tiles (every S product is complete once
+    // o_full[0] fires) for a coalesced copy to the output.
     bool have = ok && done_tiles == n && n > 0;
     if (have) {
       const bool od = wait_bar(smem_addr(&o_full[q]), 0, ctl);
@@ -479,31 +481,41 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     const float inv = l > 0.f ? 1.f / l : 0.f;
     const float lse_v = (have && l > 0.f) ? (ref + log2f(l)) * kLn2 : -INFINITY;
+    float o[kHD];
+    if (have) {
+      tmem_ld128(tO + loff, o);
+    } else {
 #pragma unroll
-    for (int c = 0; c < 4; ++c) {
-      float o[32];
-      if (have) {
-        tmem_ld32(tO + loff + c * 32, o);
-      } else {
-#pragma unroll
-        for (int e = 0; e < 32; ++e) o[e] = 0.f;
-      }
-#pragma unroll
-      for (int e = 0; e < 4; ++e)
-        *reinterpret_cast<uint4*>(sm + stage_off(rt, c * 4 + e)) =
-            make_uint4(pack2(o[e * 8] * inv, o[e * 8 + 1] * inv), pack2(o[e * 8 + 2] * inv, o[e * 8 + 3] * inv),
-                       pack2(o[e * 8 + 4] * inv, o[e * 8 + 5] * inv), pack2(o[e * 8 + 6] * inv, o[e * 8 + 7] * inv));
+      for (int e = 0; e < kHD; ++e) o[e] = 0.f;
     }
-    s_lse[rt] = row_ok ? lse_v : -INFINITY;
+    uint4* po = a.splits > 1
+                    ? a.part_o + ((size_t)(g * gridDim.x + mblk) * a.splits + split) * (kBM * (kHD / 8)) + rt
+                    : nullptr;
+#pragma unroll
+    for (int pc = 0; pc < kHD / 8; ++pc) {
+      const float* x = o + pc * 8;
+      const uint4 w = make_uint4(pack2(x[0] * inv, x[1] * inv), pack2(x[2] * inv, x[3] * inv),
+                                 pack2(x[4] * inv, x[5] * inv), pack2(x[6] * inv, x[7] * inv));
+      if (po)
+        po[pc * kBM] = w;
+      else
+        *reinterpret_cast<uint4*>(sm + stage_off(rt, pc)) = w;
+    }
+    const float lse_row = row_ok ? lse_v : -INFINITY;
+    if (po) {
+      a.part_lse[((size_t)(g * gridDim.x + mblk) * a.splits + split) * kBM + rt] = lse_row;
+      __threadfence();  // this split's rows, before the arrival below
+    } else {
+      s_lse[rt] = lse_row;
+    }
   }
-  fence_proxy_async_smem();  // staged rows -> the bulk copy below
   tc_fence_before();
   __syncthreads();
 
   // ------------------------------------------------ publish this split's partial, then merge
   const int grp_id = g * gridDim.x + mblk;
   const int cs = a.splits;
-  constexpr int kRowPieces = kHD / 8;  // 16-byte pieces of a staged row
+  constexpr int kRowPieces = kHD / 8;  // 16-byte pieces of a row
   bool merge = false;
   if (cs == 1) {
     // one split: the staged rows are the output (bf16 O / l); coalesced copy-out
@@ -518,16 +530,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     if (tid == 0) {
-      bulk_store(a.part_o + ((size_t)grp_id * cs + split) * (kBM * kRowPieces), sbase, kBM * kStageRow);
-      bulk_commit();
-    }
-    float* pl = a.part_lse + ((size_t)grp_id * cs + split) * kBM;
-    for (int x = tid; x < kBM; x += kThreads) pl[x] = s_lse[x];
-    __threadfence();
-    __syncthreads();
-    if (tid == 0) {
-      bulk_wait_all();
-      fence_proxy_async_global();  // the bulk-copied rows, before the release below
       if (!(a.inject && split == 0)) red_release_add_gpu(a.arrived + grp_id, 1);
       bool go = true;
       const long long t0 = clock64();
@@ -562,8 +564,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int row = r0 + t;
       const int64_t R = (int64_t)mblk * kBM + row;
       if (R >= M) continue;
-      const uint4* src0 = pg + stage_off(row, pc) / 16;
-      const uint4* src1 = pg + stage_off(row, pc + 1) / 16;
+      const uint4* src0 = pg + (size_t)pc * kBM + row;  // piece-major partial rows
+      const uint4* src1 = src0 + kBM;
       float acc[16];
 #pragma unroll
       for (int e = 0; e < 16; ++e) acc[e] = 0.f;
