@@ -33,9 +33,9 @@
 // in TMEM leaves shared-memory bandwidth to the S operands and the TMA ring.
 //
 // Split merge (no second kernel; the launch is cooperative, so every CTA is
-// resident): each CTA stages its normalised O rows (bf16) and per-row lse in
-// shared memory, copies them to its slot of the workspace with one bulk copy,
-// and arrives on its (row block, KV head) counter. Once all splits of the
+// resident): each CTA writes its normalised O rows (bf16, piece-major so
+// that every warp store is 512 contiguous bytes) and per-row lse to its slot
+// of the workspace and arrives on its (row block, KV head) counter. Once all splits of the
 // group have arrived, CTA k merges rows [k*ceil(256/splits), ...) with
 // weights exp(lse_s - lse) and writes the bf16 output and the final lse. With
 // a single split the staged rows are the output: the launch is not
@@ -81,7 +81,7 @@ struct TcArgs {
   int64_t P;              // cache prefix (with P_dev: its upper bound)
   const int64_t* P_dev;   // device-side prefix length, or null
   int n_cache_tiles, n_tiles, tiles_per_split, splits;
-  uint4* part_o;    // [group][split][256 rows][128] bf16 (O / l), rows as staged (swizzled 16-byte pieces)
+  uint4* part_o;    // [group][split][16 pieces][256 rows] x 8 bf16 (O / l)
   float* part_lse;  // [group][split][256]
   int* arrived;     // [group] splits that have published their partial (zeroed before launch)
   float scale_log2;
