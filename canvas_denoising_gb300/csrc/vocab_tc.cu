@@ -613,6 +613,7 @@ __global__ void __launch_bounds__(256) vocab_combine(const Params p, const __nv_
     for (int k = 0; k < kMaxSplitRegs; ++k)
       if (k < p.ksplit) part[k] = __ldcg(reinterpret_cast<const float4*>(src + k * kstride));
   }
+  const bool ovf = __ldcg(p.overflow + i) != 0;  // with the loads above, not after the reductions
   float m = -INFINITY, z = 0.f, R = -INFINITY;
   int ai = 0x7fffffff;
   const size_t rb = (size_t)i * p.n_a;
@@ -641,7 +642,6 @@ __global__ void __launch_bounds__(256) vocab_combine(const Params p, const __nv_
   __syncthreads();
   const int c0 = slice * kCombineCols;
   const int c1 = min(p.d, c0 + kCombineCols);
-  const bool ovf = p.overflow[i] != 0;
   float out_conf, out_lse;
   if (!ovf) {
     out_conf = expf(m - R) / z;
