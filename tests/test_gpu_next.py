@@ -175,3 +175,21 @@ def test_devlen_append_and_bounds(lib):
     B.kv_append_devlen(k, v, ln, kn, vn)  # 138 + 64 > 200: nothing written, length unchanged
     assert B.device_status() == B.DG_ERR_DEVICE_BOUNDS
     assert int(ln.item()) == 10 + 2 * C and torch.equal(k, before)
+
+
+def test_large_prefill_chunk_is_causal(lib):
+    """A 16384-row prompt chunk (2048 CTAs, more than fit at once): row i sees
+    only keys 0..i, so its first 2048 rows equal the 2048-row chunk's, which
+    the oracle test above checks; the lse agree as well."""
+    Hkv, Hq, hd, C, Cs = 8, 16, 128, 16384, 2048
+    k, v = synth.kv_prefix(Hkv, C, hd, 0, seed=43, device="cuda")
+    q, kn, vn = synth.canvas_qkv(C, Hq, Hkv, hd, seed=43, device="cuda")
+    _, out, lse = B.kv_append(k, v, 0, kn, vn, q_new=q)
+    k2, v2 = synth.kv_prefix(Hkv, Cs, hd, 0, seed=43, device="cuda")
+    _, out_s, lse_s = B.kv_append(k2, v2, 0, kn[:, :Cs].contiguous(), vn[:, :Cs].contiguous(),
+                                  q_new=q[:Cs].contiguous())
+    assert_rows_close(_np(out[:Cs]).reshape(Cs * Hq, hd), _np(out_s).reshape(Cs * Hq, hd), tol=1e-2,
+                      what="prefix rows")
+    assert np.abs(_np(lse[:, :Cs]) - _np(lse_s)).max() <= 1e-3
+    assert np.isfinite(_np(out)).all() and np.isfinite(_np(lse)).all()
+    assert B.device_status() == B.DG_OK
