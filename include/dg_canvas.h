@@ -18,6 +18,12 @@
  *   dg_kv_append     -- "Architecture..." prefill mode and "Multi-canvas
  *                       sampling": each finalised canvas is appended to the
  *                       KV cache with causal attention.
+ * Further calls, each documented in its section below: dg_vocab_step_renoise
+ * (the vocabulary step with the re-noise fused in), dg_vocab_step_plan,
+ * dg_canvas_attn_noalloc, the calls next to the step (dg_selfcond_input,
+ * dg_token_prob, dg_unmask, dg_canvas_fill, dg_count_flags), the device-side
+ * cache length variants (*_devlen, *_devpos) and the test hook
+ * dg_debug_inject.
  *
  * Conventions shared by every call
  *   - Pointers named as tensors are DEVICE pointers owned by the caller, in
