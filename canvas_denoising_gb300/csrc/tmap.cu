@@ -31,6 +31,7 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 struct Key {
   const void* base;
   int rank;
+  int swizzle;
   uint64_t dims[5], strides[4];
   uint32_t box[5];
   bool operator==(const Key& o) const { return memcmp(this, &o, sizeof(Key)) == 0; }
@@ -47,15 +48,14 @@ std::mutex g_mu;
 Entry g_cache[kSlots];
 int g_next = 0;
 
-}  // namespace
-
-bool tmap_bf16_sw128(CUtensorMap* out, const void* base, int rank, const uint64_t* dims, const uint64_t* strides,
-                     const uint32_t* box) {
+bool encode(CUtensorMap* out, const void* base, int rank, const uint64_t* dims, const uint64_t* strides,
+            const uint32_t* box, CUtensorMapSwizzle swizzle) {
   if (rank < 2 || rank > 5) return false;
   Key k;
   memset(&k, 0, sizeof(k));
   k.base = base;
   k.rank = rank;
+  k.swizzle = (int)swizzle;
   for (int i = 0; i < rank; ++i) {
     k.dims[i] = dims[i];
     k.box[i] = box[i];
@@ -80,7 +80,7 @@ bool tmap_bf16_sw128(CUtensorMap* out, const void* base, int rank, const uint64_
   for (int i = 0; i < rank - 1; ++i) s[i] = strides[i];
   CUtensorMap m;
   if (fn(&m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (cuuint32_t)rank, const_cast<void*>(base), d, s, b, e,
-         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+         CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
     return false;
   std::lock_guard<std::mutex> lk(g_mu);
@@ -90,6 +90,18 @@ bool tmap_bf16_sw128(CUtensorMap* out, const void* base, int rank, const uint64_
   g_next = (g_next + 1) % kSlots;
   *out = m;
   return true;
+}
+
+}  // namespace
+
+bool tmap_bf16_sw128(CUtensorMap* out, const void* base, int rank, const uint64_t* dims, const uint64_t* strides,
+                     const uint32_t* box) {
+  return encode(out, base, rank, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
+bool tmap_bf16_plain(CUtensorMap* out, const void* base, int rank, const uint64_t* dims, const uint64_t* strides,
+                     const uint32_t* box) {
+  return encode(out, base, rank, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_NONE);
 }
 
 }  // namespace dg

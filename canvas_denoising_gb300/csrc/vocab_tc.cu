@@ -168,6 +168,9 @@ struct Params {
   int inject;                  // test injection: tile 0's ready flag is never released
   long long wait_cycles;       // bound of every wait
   int* status;
+  // paired form only: producer pairs, and the consumer pairs' d-slicing
+  // (n_full slices of 512 columns, then a remainder of `rem` columns; see consumer_slice)
+  int n_pa, n_full, rem, n_fullx;
 };
 
 __device__ __forceinline__ bool aborted(const int* f) { return *(volatile const int*)f != 0; }
@@ -584,6 +587,391 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+// ============================================================================ paired form
+// The same two roles on CTA pairs (clusters of two, cta_group::2). One MMA of
+// M = 256 covers all canvas rows: each CTA of the pair holds 128 rows of the A
+// operand and half of the B operand's columns, so per unit of work each SM
+// reads half as much B from shared memory as in vocab_main, and each CTA's
+// accumulator holds only its own 128 rows.
+//  * Producer pair: tile t of 256 ids; CTA r loads H rows [128r, 128r+128)
+//    and E ids [256t + 128r, +128) per 64-deep k-step (32 KB per stage, six
+//    stages). Its accumulator, 128 rows x 256 ids, is 256 TMEM columns, so
+//    two buffers fit: the epilogue of tile j overlaps the MMAs of tile j+1.
+//    Epilogue warp w reads one 128-id half (hc) of its row in one load and
+//    keeps statistics per (pair, hc) slot.
+//  * Consumer pair: a d-slice of up to 512 columns (two MMAs of N <= 256,
+//    each CTA holding half of each N) and one residue class of tiles; the
+//    pairs of a narrow remainder slice take two residue classes each, so that
+//    every consumer pair carries about the same work.
+// Loads of both CTAs complete on the even CTA's "full" barrier (it alone
+// issues MMAs); commits arrive on both CTAs' barriers.
+constexpr int kRingBytes = 196608;   // operand ring per CTA
+constexpr int kMaxRing = 6;
+constexpr uint32_t kStageA2 = 32768u;  // producer stage per CTA: H [128 x 64] + E [128 ids x 64]
+constexpr int kRingA2 = kRingBytes / (int)kStageA2;
+constexpr int kEpiWarps = 8;
+
+// d-slice and residue classes of consumer pair c: n_fullx slices per residue
+// class ra (n_full of 512 columns, then possibly the remainder); pairs past
+// ksplit * n_fullx serve a narrow remainder slice (rem <= 256 columns, next to
+// full slices) for residues ra and rb = ra + 1 (rb = -1: none).
+__device__ __forceinline__ void consumer_slice(const Params& p, int c, int& d0, int& nd, int& ra, int& rb) {
+  const int n_res = p.ksplit * p.n_fullx;
+  if (c < n_res) {
+    const int sl = c % p.n_fullx;
+    ra = c / p.n_fullx;
+    rb = -1;
+    d0 = sl * 512;
+    nd = sl < p.n_full ? 512 : p.rem;
+  } else {
+    const int h = c - n_res;
+    ra = 2 * h;
+    rb = 2 * h + 1 < p.ksplit ? 2 * h + 1 : -1;
+    d0 = p.n_full * 512;
+    nd = p.rem;
+  }
+}
+
+// u-th tile of a consumer pair (ascending; may exceed n_vt, which callers skip).
+__device__ __forceinline__ int consumer_tile(int u, int ra, int rb, int ks) {
+  return rb < 0 ? ra + u * ks : (u >> 1) * ks + ((u & 1) ? rb : ra);
+}
+
+__device__ __forceinline__ void pair_load(uint32_t dst, const CUtensorMap* map, int x, int y, uint32_t bar,
+                                          bool hint, uint64_t pol) {
+  if (hint)
+    tma_load_2d_pair_hint(dst, map, x, y, bar, pol);
+  else
+    tma_load_2d_pair(dst, map, x, y, bar);
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    vocab_pair(const __grid_constant__ CUtensorMap tm_h, const __grid_constant__ CUtensorMap tm_ek,
+               const __grid_constant__ CUtensorMap tm_emn, const __grid_constant__ CUtensorMap tm_p, const Params p) {
+  extern __shared__ __align__(1024) uint8_t smem_dyn[];
+  __shared__ __align__(8) uint64_t bar_full[kMaxRing], bar_empty[kMaxRing], bar_tfull[2], bar_tempty[2], bar_drain;
+  __shared__ uint32_t tmem_slot;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  uint8_t* ring = (uint8_t*)(((uintptr_t)smem_dyn + 1023) & ~(uintptr_t)1023);
+  const uint32_t s_base = smem_addr(ring);
+  const uint32_t rank = cluster_ctarank();
+  const bool leader = rank == 0;
+  const int pair = (int)(blockIdx.x >> 1);
+  const bool is_a = pair < p.n_pa;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kMaxRing; ++s) {
+      mbar_init(smem_addr(&bar_full[s]), 1);
+      mbar_init(smem_addr(&bar_empty[s]), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(smem_addr(&bar_tfull[b]), 1);
+      mbar_init(smem_addr(&bar_tempty[b]), 2 * kEpiWarps);
+    }
+    mbar_init(smem_addr(&bar_drain), 1);
+    fence_mbar_init();
+    prefetch_tmap(&tm_h);
+    prefetch_tmap(&tm_ek);
+    prefetch_tmap(&tm_emn);
+    prefetch_tmap(&tm_p);
+  }
+  if (warp == 1) {
+    tmem_alloc_pair(smem_addr(&tmem_slot), 512);
+    tmem_relinquish_pair();
+  }
+  tc_fence_before();
+  cluster_sync();  // both CTAs' barriers initialised and TMEM allocated
+  tc_fence_after();
+  const uint32_t tmem = tmem_slot;
+
+  if (is_a) {
+    // ===================================================== producer pair: GEMM1 + softmax epilogue
+    const int a = pair;
+    const int n_my = a < p.n_vt ? (p.n_vt - a + p.n_pa - 1) / p.n_pa : 0;
+    const int ksteps_d = p.d / kBK;
+    if (warp == 0) {
+      if (lane == 0 && n_my > 0) {
+        const uint64_t pol = policy_evict_last();
+        int stage = 0;
+        uint32_t ph = 0;
+        bool ok = true;
+        for (int j = 0; j < n_my && ok; ++j) {
+          const int t = a + j * p.n_pa;
+          for (int ks = 0; ks < ksteps_d; ++ks) {
+            if (!wait_bar(smem_addr(&bar_empty[stage]), ph ^ 1, p)) { ok = false; break; }
+            const uint32_t fb = smem_addr(&bar_full[stage]);
+            const uint32_t fl = mapa_shared(fb, 0);
+            const uint32_t sb = s_base + stage * kStageA2;
+            if (leader) mbar_expect_tx(fb, 2 * kStageA2);
+            pair_load(sb, &tm_h, ks * kBK, (int)rank * 128, fl, p.l2hint, pol);
+            pair_load(sb + 16384, &tm_ek, ks * kBK, t * kVT + (int)rank * 128, fl, p.l2hint, pol);
+            if (++stage == kRingA2) { stage = 0; ph ^= 1; }
+          }
+        }
+      }
+      __syncwarp();
+    } else if (warp == 1) {
+      if (leader && lane == 0 && n_my > 0) {
+        const uint32_t idesc = idesc_bf16_f32(256, kVT, 0, 0);
+        int stage = 0;
+        uint32_t ph = 0;
+        bool ok = true;
+        for (int j = 0; j < n_my && ok; ++j) {
+          const int b = j & 1;
+          // accumulator b must have been read out (tile j-2) by both CTAs' epilogues
+          if (!wait_bar(smem_addr(&bar_tempty[b]), ((uint32_t)(j >> 1) & 1u) ^ 1u, p)) break;
+          tc_fence_after();
+          for (int ks = 0; ks < ksteps_d; ++ks) {
+            if (!wait_bar(smem_addr(&bar_full[stage]), ph, p)) { ok = false; break; }
+            tc_fence_after();
+            const uint32_t sb = s_base + stage * kStageA2;
+#pragma unroll
+            for (int k = 0; k < kBK / 16; ++k)
+              mma_bf16_pair(tmem + b * 256, sdesc_sw128(sb + k * 32, 0, 1024), sdesc_sw128(sb + 16384 + k * 32, 0, 1024),
+                            idesc, (ks | k) != 0);
+            mma_commit_pair_mc(smem_addr(&bar_empty[stage]), 3);
+            if (++stage == kRingA2) { stage = 0; ph ^= 1; }
+          }
+          if (ok) mma_commit_pair_mc(smem_addr(&bar_tfull[b]), 3);
+        }
+        mma_commit_pair_mc(smem_addr(&bar_drain), 1);
+        drain_bar(smem_addr(&bar_drain), 0, p);
+      }
+      __syncwarp();
+    } else {
+      // epilogue warps 2..9: id half hc of the tile, TMEM lane quarter q
+      const int hc = (warp - 2) >> 2;
+      const int q = warp & 3;
+      const int r = q * 32 + lane;  // row within this CTA's half = TMEM lane
+      const int i = (int)rank * 128 + r;
+      const int slot = a * 2 + hc;
+      const uint32_t tl = tmem + ((uint32_t)(q * 32) << 16) + hc * 128;
+      float R2 = 0.f, lim2 = 0.f;
+      float m_run = -INFINITY, z_run = 0.f;
+      int a_run = 0x7fffffff;
+      bool ovf = false;
+      bool ok = true;
+      if (n_my == 0) {
+        p.smax[(size_t)i * p.n_a + slot] = -INFINITY;
+        __threadfence();
+        epi_sync();
+        if (threadIdx.x == 64) red_release_add_gpu(p.ref_count, 1);
+      }
+      for (int j = 0; j < n_my && ok; ++j) {
+        const int t = a + j * p.n_pa;
+        const int b = j & 1;
+        const bool got = wait_bar(smem_addr(&bar_tfull[b]), (uint32_t)(j >> 1) & 1u, p);
+        if (epi_any(!got)) { ok = false; break; }
+        tc_fence_after();
+        float v[128];
+        tmem_ld128(tl + b * 256, v);
+        // every logit of this half-tile is in registers: hand the buffer back
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_addr(&bar_tempty[b]), 0));
+        const int vb = t * kVT + hc * 128;
+        if (vb + 128 > p.V) {
+#pragma unroll
+          for (int e = 0; e < 128; ++e)
+            if (vb + e >= p.V) v[e] = -INFINITY;
+        }
+        float bm[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) bm[e] = fmaxf(v[e], v[120 + e]);
+#pragma unroll
+        for (int bb = 8; bb < 120; bb += 16)
+#pragma unroll
+          for (int e = 0; e < 8; ++e) bm[e] = max3(bm[e], v[bb + e], v[bb + 8 + e]);
+        const float cm = max3(max3(bm[0], bm[1], bm[2]), max3(bm[3], bm[4], bm[5]), fmaxf(bm[6], bm[7]));
+        if (j == 0) {
+          // this slot's first half-tile is its sample -> grid-wide reference
+          p.smax[(size_t)i * p.n_a + slot] = cm;
+          __threadfence();
+          epi_sync();
+          if (threadIdx.x == 64) red_release_add_gpu(p.ref_count, 1);
+          const bool refd = wait_flag(p.ref_count, 2 * p.n_pa, p);
+          if (epi_any(!refd)) { ok = false; break; }
+          float R = -INFINITY;
+          const float* sm_row = p.smax + (size_t)i * p.n_a;
+          for (int aa = 0; aa < p.n_a; ++aa) R = fmaxf(R, __ldcg(sm_row + aa));
+          R2 = R * kLog2e;
+          lim2 = (R + kTau) * kLog2e;
+        }
+        if (cm > m_run) {
+          int ci = 127;
+#pragma unroll
+          for (int e = 127; e >= 0; --e)
+            if (v[e] == cm) ci = e;
+          m_run = cm;
+          a_run = vb + ci;
+        }
+        if (cm * kLog2e > lim2) ovf = true;
+        float zs[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) zs[e] = 0.f;
+        // P blocks [t][sub-tile of 64 ids][row half = rank], pre-swizzled K-major
+        uint8_t* prow = p.pbuf + ((size_t)((t * 4 + hc * 2) * 2 + (int)rank)) * kTileBytes + (size_t)r * 128;
+#pragma unroll
+        for (int e8 = 0; e8 < 16; ++e8) {
+          float pe[8];
+#pragma unroll
+          for (int f = 0; f < 8; f += 2) {
+            float x0, x1;
+            fma2(x0, x1, v[e8 * 8 + f], v[e8 * 8 + f + 1], kLog2e, kLog2e, -R2, -R2);
+            pe[f] = ex2_approx(x0);  // masked ids: exp2(-inf) = 0
+            pe[f + 1] = ex2_approx(x1);
+            add2(zs[f], zs[f + 1], pe[f], pe[f + 1]);
+          }
+          const int sub = e8 >> 3, piece = e8 & 7;
+          uint8_t* dst = prow + (size_t)sub * 2 * kTileBytes + ((piece ^ (r & 7)) << 4);
+          *reinterpret_cast<uint4*>(dst) =
+              make_uint4(pack2(pe[0], pe[1]), pack2(pe[2], pe[3]), pack2(pe[4], pe[5]), pack2(pe[6], pe[7]));
+        }
+        z_run += ((zs[0] + zs[1]) + (zs[2] + zs[3])) + ((zs[4] + zs[5]) + (zs[6] + zs[7]));
+        // publish this CTA's half of the P tile (consumers wait for both halves)
+        fence_proxy_async_global();
+        __threadfence();
+        epi_sync();
+        if (threadIdx.x == 64 && !(p.inject && t == 0)) red_release_add_gpu(p.ready + t, 1);
+      }
+      if (i < p.C) {
+        p.am[(size_t)i * p.n_a + slot] = m_run;
+        p.aa[(size_t)i * p.n_a + slot] = a_run;
+        p.az[(size_t)i * p.n_a + slot] = z_run;
+        if (ovf) p.overflow[i] = 1;
+      }
+    }
+  } else {
+    // ===================================================== consumer pair: GEMM2 (S += P . E)
+    int d0, nd, ra, rb;
+    consumer_slice(p, pair - p.n_pa, d0, nd, ra, rb);
+    const int n_mma = nd > 256 ? 2 : 1;
+    const int N0 = nd >= 256 ? 256 : (nd <= 128 ? 128 : 256);
+    const int N1 = n_mma == 2 ? (nd - 256 <= 128 ? 128 : 256) : 0;
+    const uint32_t e1_off = 16384u + (uint32_t)(N0 / 128) * 8192u;  // E block of the second MMA
+    const uint32_t stage_bytes = e1_off + (uint32_t)(N1 / 128) * 8192u;
+    const int n_stages = kRingBytes / (int)stage_bytes < kMaxRing ? kRingBytes / (int)stage_bytes : kMaxRing;
+    const int cnt_a = ra < p.n_vt ? (p.n_vt - ra + p.ksplit - 1) / p.ksplit : 0;
+    const int cnt_b = rb >= 0 && rb < p.n_vt ? (p.n_vt - rb + p.ksplit - 1) / p.ksplit : 0;
+    const int n_iter = rb < 0 ? cnt_a : 2 * cnt_a;
+    const int n_my = cnt_a + cnt_b;
+    if (warp == 0) {
+      if (lane == 0 && n_my > 0) {
+        const uint64_t pol = policy_evict_first();
+        int stage = 0;
+        uint32_t ph = 0;
+        bool ok = true;
+        for (int u = 0; u < n_iter && ok; ++u) {
+          const int t = consumer_tile(u, ra, rb, p.ksplit);
+          if (t >= p.n_vt) continue;
+          if (!wait_flag(p.ready + t, 2, p)) break;
+          fence_proxy_async_global();
+          for (int ks = 0; ks < kVT / 64; ++ks) {
+            if (!wait_bar(smem_addr(&bar_empty[stage]), ph ^ 1, p)) { ok = false; break; }
+            const uint32_t fb = smem_addr(&bar_full[stage]);
+            const uint32_t fl = mapa_shared(fb, 0);
+            const uint32_t sb = s_base + stage * stage_bytes;
+            if (leader) mbar_expect_tx(fb, 2 * stage_bytes);
+            pair_load(sb, &tm_p, 0, ((t * 4 + ks) * 2 + (int)rank) * 128, fl, p.l2hint, pol);
+            for (int m = 0; m < n_mma; ++m) {
+              const int Nm = m ? N1 : N0;
+              const uint32_t eb = sb + (m ? e1_off : 16384u);
+              for (int bx = 0; bx < Nm / 128; ++bx)
+                pair_load(eb + bx * 8192, &tm_emn, d0 + m * 256 + (int)rank * (Nm / 2) + bx * 64, t * kVT + ks * 64,
+                          fl, p.l2hint, pol);
+            }
+            if (++stage == n_stages) { stage = 0; ph ^= 1; }
+          }
+        }
+      }
+      __syncwarp();
+    } else if (warp == 1) {
+      if (leader && lane == 0 && n_my > 0) {
+        const uint32_t id0 = idesc_bf16_f32(256, N0, 0, 1);
+        const uint32_t id1 = idesc_bf16_f32(256, N1 ? N1 : 128, 0, 1);
+        int stage = 0;
+        uint32_t ph = 0;
+        bool ok = true, first = true;
+        for (int u = 0; u < n_iter && ok; ++u) {
+          const int t = consumer_tile(u, ra, rb, p.ksplit);
+          if (t >= p.n_vt) continue;
+          for (int ks = 0; ks < kVT / 64; ++ks) {
+            if (!wait_bar(smem_addr(&bar_full[stage]), ph, p)) { ok = false; break; }
+            tc_fence_after();
+            const uint32_t sb = s_base + stage * stage_bytes;
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              const uint32_t acc = (first && ks == 0 && k == 0) ? 0u : 1u;
+              const uint64_t adesc = sdesc_sw128(sb + k * 32, 0, 1024);
+              mma_bf16_pair(tmem, adesc, sdesc_sw128(sb + 16384 + k * 2048, 8192, 1024), id0, acc);
+              if (n_mma == 2) mma_bf16_pair(tmem + 256, adesc, sdesc_sw128(sb + e1_off + k * 2048, 8192, 1024), id1, acc);
+            }
+            mma_commit_pair_mc(smem_addr(&bar_empty[stage]), 3);
+            if (++stage == n_stages) { stage = 0; ph ^= 1; }
+          }
+          first = false;
+        }
+        mma_commit_pair_mc(smem_addr(&bar_tfull[0]), 3);
+        mma_commit_pair_mc(smem_addr(&bar_drain), 1);
+        drain_bar(smem_addr(&bar_drain), 0, p);
+      }
+      __syncwarp();
+    } else {
+      // epilogue: warp w reads accumulator m = (w-2)/4 (columns d0 + 256m ...) for its lane quarter
+      const int q = warp & 3;
+      const int m = (warp - 2) >> 2;
+      const int r = q * 32 + lane;
+      const int i = (int)rank * 128 + r;
+      if (m < n_mma) {
+        bool have = n_my > 0;
+        if (n_my > 0) {
+          bool got = wait_bar(smem_addr(&bar_tfull[0]), 0, p);
+          got = __all_sync(0xffffffffu, got);  // tcgen05.ld below is warp-collective
+          have = got;
+          tc_fence_after();
+        }
+        const int Nm = m ? N1 : N0;
+        const int cend = d0 + nd;
+        float* dst = p.cpart + ((size_t)ra * 256 + i) * p.d;
+        float* dz = rb >= 0 ? p.cpart + ((size_t)rb * 256 + i) * p.d : nullptr;
+        for (int cc = 0; cc < Nm / 32; ++cc) {
+          const int col = d0 + m * 256 + cc * 32;
+          float v[32];
+          if (have) {
+            tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + m * 256 + cc * 32, v);
+          } else {
+#pragma unroll
+            for (int e = 0; e < 32; ++e) v[e] = 0.f;
+          }
+          if (i < p.C && col < cend) {
+#pragma unroll
+            for (int e = 0; e < 32; e += 4) {
+              *reinterpret_cast<float4*>(dst + col + e) = make_float4(v[e], v[e + 1], v[e + 2], v[e + 3]);
+              if (dz) *reinterpret_cast<float4*>(dz + col + e) = make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+          }
+        }
+      }
+    }
+  }
+  // After a timeout or abort, loads this CTA issued may still be landing (their
+  // barrier is the even CTA's): give them time before the pair's shared memory
+  // is released.
+  if (warp == 0 && lane == 0 && aborted(p.abort_flag)) {
+    const long long t0 = clock64();
+    while (clock64() - t0 < 4000000ll) {
+    }
+  }
+  __syncwarp();
+  tc_fence_before();
+  cluster_sync();  // the even CTA's MMAs have finished with both CTAs' shared memory and TMEM
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc_pair(tmem, 512);
+  }
+}
+
 // Merge producer statistics and consumer partials for one canvas row and one
 // slice of kCombineCols columns of S. Row statistics are contiguous per row
 // ([row][producer]); S partials are read once, coalesced. A row flagged by the
@@ -740,9 +1128,113 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows, ui
   return tmap_bf16_sw128(m, base, 2, dims, strides, box);
 }
 
+// ---------------------------------------------------------------- paired form: plan
+// Clusters of two vocab_pair CTAs that fit on the device at once (0: none).
+// Without a device (a host-only plan query) the plan assumes every SM pairs up.
+int pair_capacity() {
+  static std::once_flag once;
+  static int cap = 0;
+  std::call_once(once, [] {
+    int dev = 0, nsm = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || nsm <= 0) {
+      cudaGetLastError();
+      cap = num_sms() / 2;
+      return;
+    }
+    const size_t smem = (size_t)kRingBytes + 1024;
+    if (cudaFuncSetAttribute(vocab_pair, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess) {
+      cudaGetLastError();
+      return;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2 * (nsm / 2));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeClusterDimension;
+    at[0].val.clusterDim.x = 2;
+    at[0].val.clusterDim.y = 1;
+    at[0].val.clusterDim.z = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, vocab_pair, &cfg) != cudaSuccess) {
+      cudaGetLastError();
+      n = 0;
+    }
+    cap = n;
+  });
+  return cap;
+}
+
+struct PairPlan {
+  int n_vt, n_pa, n_pc, ksplit, n_full, rem, n_fullx;
+};
+
+// Splits the pairs between the roles and picks the number of vocabulary residue
+// classes (ksplit) that maximises the tile rate, in units of one producer
+// pair's rate: producers give n_pa; a consumer pair of width w finishes a tile
+// in w/d of a producer tile-time, so the residue classes sustain ksplit * d / w
+// (remainder pairs, serving two classes, ksplit * d / (2 rem)). False if no
+// split fits.
+bool make_pair_plan(int V, int d, PairPlan* q) {
+  static const char* single = getenv("DG_VOCAB_SINGLE_SM");
+  if (single && single[0] == '1') return false;
+  const int pairs = pair_capacity() < num_sms() / 2 ? pair_capacity() : num_sms() / 2;
+  q->n_vt = (V + kVT - 1) / kVT;
+  q->n_full = d / 512;
+  q->rem = d % 512;
+  // A remainder of at most 256 columns next to full slices gets pairs that serve
+  // two residue classes; otherwise the remainder is one more per-class slice.
+  const bool half = q->rem > 0 && q->rem <= 256 && q->n_full > 0;
+  q->n_fullx = q->n_full + (q->rem > 0 && !half ? 1 : 0);
+  const double wmax = q->n_full > 0 ? 512.0 : (double)q->rem;
+  double best = -1.0;
+  for (int ks = 1; ks <= 32 && ks <= q->n_vt; ++ks) {
+    const int n_pc = ks * q->n_fullx + (half ? (ks + 1) / 2 : 0);
+    if (n_pc >= pairs) break;
+    const int n_pa = pairs - n_pc < q->n_vt ? pairs - n_pc : q->n_vt;
+    double cons = 1e30;
+    if (q->n_fullx > 0) cons = fmin(cons, ks * (double)d / wmax);
+    if (half) cons = fmin(cons, ks * (double)d / (2.0 * q->rem));
+    const double rate = fmin((double)n_pa, cons);
+    if (rate > best + 1e-9) {
+      best = rate;
+      q->ksplit = ks;
+      q->n_pc = n_pc;
+      q->n_pa = n_pa;
+    }
+  }
+  return best > 0.0;
+}
+
+// The single-SM plan's fields that size the workspace, for the paired form.
+Plan as_plan(const PairPlan& q) {
+  Plan p = {};
+  p.n_rh = 2;
+  p.n_vt = q.n_vt;
+  p.ksplit = q.ksplit;
+  p.n_a = 2 * q.n_pa;  // statistics slots: (pair, id half)
+  p.n_c = 2 * q.n_pc;
+  p.n_dt = 0;
+  p.window = 1 << 30;
+  return p;
+}
+
 }  // namespace
 
 int vocab_tc_plan(int C, int V, int d, int* out) {
+  PairPlan q;
+  if (make_pair_plan(V, d, &q)) {
+    out[0] = 2 * q.n_pa;
+    out[1] = 2 * q.n_pc;
+    out[2] = q.ksplit;
+    out[3] = 1;  // CTA pairs (clusters of two)
+    out[4] = 2 * (q.n_pa + q.n_pc);
+    out[5] = q.n_vt;
+    return DG_OK;
+  }
   const Plan pl = make_plan(C, V, d);
   out[0] = pl.n_a;
   out[1] = pl.n_c;
@@ -754,6 +1246,8 @@ int vocab_tc_plan(int C, int V, int d, int* out) {
 }
 
 size_t vocab_tc_workspace(int C, int V, int d) {
+  PairPlan q;
+  if (make_pair_plan(V, d, &q)) return make_layout(as_plan(q), d).total;
   Plan pl = make_plan(C, V, d);
   return make_layout(pl, d).total;
 }
@@ -761,19 +1255,33 @@ size_t vocab_tc_workspace(int C, int V, int d) {
 int vocab_tc_launch(const __nv_bfloat16* h, const __nv_bfloat16* emb, int C, int V, int d, int32_t* argmax,
                     float* conf, float* lse, __nv_bfloat16* selfcond, void* ws, size_t ws_bytes, cudaStream_t s,
                     const RenoiseArgs* rn) {
-  const Plan pl = make_plan(C, V, d);
+  PairPlan pq;
+  const bool pairs = make_pair_plan(V, d, &pq);
+  const Plan pl = pairs ? as_plan(pq) : make_plan(C, V, d);
   const Layout L = make_layout(pl, d);
   if (ws_bytes < L.total) return DG_ERR_WORKSPACE;
   int* st = status_ptr();
   if (!st) return DG_ERR_CUDA;
-  CUtensorMap tm_h, tm_ek, tm_emn;
-  if (!make_map(&tm_h, h, d, C, 128) || !make_map(&tm_ek, emb, d, V, kVT) || !make_map(&tm_emn, emb, d, V, 64))
+  CUtensorMap tm_h, tm_ek, tm_emn, tm_p;
+  if (!make_map(&tm_h, h, d, C, 128) || !make_map(&tm_ek, emb, d, V, pairs ? 128 : kVT) ||
+      !make_map(&tm_emn, emb, d, V, 64))
     return DG_ERR_CUDA;
+  if (pairs) {
+    // the P ring as rows of 64 bf16: one box = one pre-swizzled 16 KB block
+    const uint64_t dims[2] = {64, (uint64_t)pl.n_vt * 4 * 2 * 128};
+    const uint64_t strides[1] = {128};
+    const uint32_t box[2] = {64, 128};
+    if (!tmap_bf16_plain(&tm_p, (uint8_t*)ws + L.pbuf, 2, dims, strides, box)) return DG_ERR_CUDA;
+  }
   uint8_t* w = (uint8_t*)ws;
   Params p;
   p.C = C; p.V = V; p.d = d;
   p.n_rh = pl.n_rh; p.n_dt = pl.n_dt; p.n_vt = pl.n_vt; p.ksplit = pl.ksplit; p.n_a = pl.n_a;
   p.window = pl.window;
+  p.n_pa = pairs ? pq.n_pa : 0;
+  p.n_full = pairs ? pq.n_full : 0;
+  p.rem = pairs ? pq.rem : 0;
+  p.n_fullx = pairs ? pq.n_fullx : 0;
   // L2 eviction hints on by default (measured: DRAM reads 725 -> 601 MB at
   // V=65536); DG_VOCAB_L2HINT=2 turns them off for comparison.
   static const int l2hint = env_int("DG_VOCAB_L2HINT", 1);
@@ -803,6 +1311,24 @@ int vocab_tc_launch(const __nv_bfloat16* h, const __nv_bfloat16* emb, int C, int
   p.wait_cycles = inj.wait_cycles > 0 ? inj.wait_cycles : kTimeoutCycles;
   DG_CUDA_TRY(cudaMemsetAsync(flags, 0, L.flag_bytes, s));
 
+  if (pairs) {
+    const size_t psmem = (size_t)kRingBytes + 1024;  // attribute set by pair_capacity()
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2 * (pq.n_pa + pq.n_pc));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = psmem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = 2;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    DG_CUDA_TRY(cudaLaunchKernelEx(&cfg, vocab_pair, tm_h, tm_ek, tm_emn, tm_p, p));
+  } else {
   const size_t smem = (size_t)kStages * kStageBytes + 1024;
   static std::once_flag attr_once;
   static cudaError_t attr_err = cudaSuccess;
@@ -822,6 +1348,7 @@ int vocab_tc_launch(const __nv_bfloat16* h, const __nv_bfloat16* emb, int C, int
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   DG_CUDA_TRY(cudaLaunchKernelEx(&cfg, vocab_main, tm_h, tm_ek, tm_emn, p));
+  }
 
   dim3 cgrid(C, (d + kCombineCols - 1) / kCombineCols);
   const size_t csmem = (size_t)d * sizeof(float);

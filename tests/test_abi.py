@@ -106,7 +106,12 @@ def test_vocab_plan_is_a_host_query(lib):
     buf = (ctypes.c_int32 * 6)()
     assert lib.dg_vocab_step_plan(256, 262144, 2816, B.DG_BF16, ctypes.cast(buf, ctypes.c_void_p)) == B.DG_OK
     n_a, n_c, ks, pair, grid, n_vt = list(buf)
-    assert n_vt == 1024 and n_c % 11 == 0 and n_c // 11 == ks and n_a + n_c <= grid <= n_a + n_c + 1
+    assert n_vt == 1024 and n_a + n_c == grid
+    if pair:
+        # CTA pairs: 2816 = 5 slices of 512 + 256; the 256-wide slice's pairs serve two residue classes
+        assert n_a % 2 == 0 and n_c == 2 * (5 * ks + (ks + 1) // 2) and grid <= 152
+    else:
+        assert n_c % 11 == 0 and n_c // 11 == ks
     assert lib.dg_vocab_step_plan(256, 262144, 2800, B.DG_BF16, ctypes.cast(buf, ctypes.c_void_p)) == B.DG_ERR_INVALID_ARG
 
 

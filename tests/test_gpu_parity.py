@@ -2,6 +2,7 @@
 bytes. Sizes span several tiles and a ragged tail; the full-size workloads
 are checked on sampled rows."""
 import math
+import os
 
 import numpy as np
 import pytest
@@ -187,6 +188,13 @@ def _check_vocab(h, emb, res, ref):
     assert_rows_close(sc, ref["selfcond"], what="selfcond")
 
 
+def test_vocab_form_follows_environment(lib):
+    """CTA pairs unless DG_VOCAB_SINGLE_SM=1 selects the single-SM kernel (the
+    form used where two-CTA clusters cannot be placed)."""
+    want = 0 if os.environ.get("DG_VOCAB_SINGLE_SM") == "1" else 1
+    assert B.vocab_step_plan(256, 262144, 2816)["cluster_pairs"] == want
+
+
 @pytest.mark.parametrize("C,V,d,alpha,std", [
     (256, 1000, 128, 0.0, 0.3),       # ragged vocabulary tail, every tile a sample tile
     (256, 40000, 256, 4.0, 0.1),      # hundreds of tiles, most past the sample
@@ -194,6 +202,8 @@ def _check_vocab(h, emb, res, ref):
     (77, 33333, 192, 3.0, 0.1),       # one row half
     (256, 32768, 1024, 26.0, 0.02),   # the 32k-vocabulary workload's shapes
     (1, 4096, 64, 0.0, 1.0),
+    (256, 20000, 640, 3.0, 0.1),      # a 128-column remainder next to a full 512-column slice
+    (130, 7000, 768, 2.0, 0.1),       # a 256-column remainder; two rows in the second row half
 ])
 def test_vocab_step_bf16(lib, C, V, d, alpha, std):
     h, emb = _vocab_case(C, V, d, seed=C + V, alpha=alpha, std=std)

@@ -1,0 +1,22 @@
+"""The single-SM form of the vocabulary step (vocab_main: one CTA per role
+unit, used where two-CTA clusters cannot be placed) against the oracle: the
+vocabulary parity cases re-run in a child process with DG_VOCAB_SINGLE_SM=1
+(the library reads the switch once per process)."""
+import os
+import subprocess
+import sys
+
+import pytest
+
+pytestmark = pytest.mark.gpu
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def test_single_sm_form_matches_the_oracle():
+    env = dict(os.environ, DG_VOCAB_SINGLE_SM="1")
+    r = subprocess.run([sys.executable, "-m", "pytest", "-q", "-x", "-m", "gpu", "-p", "no:cacheprovider",
+                        "tests/test_gpu_parity.py", "-k", "vocab"],
+                       env=env, cwd=ROOT, capture_output=True, text=True, timeout=900)
+    assert r.returncode == 0, r.stdout[-3000:] + r.stderr[-2000:]
+    assert " passed" in r.stdout
