@@ -38,6 +38,7 @@
 #include <cudaTypedefs.h>
 #include <math.h>
 #include <stdlib.h>
+#include <string.h>
 
 #include <mutex>
 
@@ -170,7 +171,11 @@ struct Params {
   int* status;
   // paired form only: producer pairs, and the consumer pairs' d-slicing
   // (n_full slices of 512 columns, then a remainder of `rem` columns; see consumer_slice)
-  int n_pa, n_full, rem, n_fullx;
+  int n_pa, n_full, rem, n_fullx, cw;
+  // paired form: L2 policy per operand stream (H, producer E, P, consumer E):
+  // 0 none, 1 evict_last, 2 evict_first, 3 evict_normal
+  int pol[4];
+  int ring_bytes;  // paired form: operand ring per CTA (a multiple of 32 KB)
 };
 
 __device__ __forceinline__ bool aborted(const int* f) { return *(volatile const int*)f != 0; }
@@ -605,29 +610,28 @@ __global__ void __launch_bounds__(kThreads, 1)
 //    every consumer pair carries about the same work.
 // Loads of both CTAs complete on the even CTA's "full" barrier (it alone
 // issues MMAs); commits arrive on both CTAs' barriers.
-constexpr int kRingBytes = 196608;   // operand ring per CTA
+constexpr int kRingBytes = 196608;   // operand ring per CTA (6 producer stages; 7 measured no faster)
 constexpr int kMaxRing = 6;
 constexpr uint32_t kStageA2 = 32768u;  // producer stage per CTA: H [128 x 64] + E [128 ids x 64]
-constexpr int kRingA2 = kRingBytes / (int)kStageA2;
 constexpr int kEpiWarps = 8;
 
 // d-slice and residue classes of consumer pair c: n_fullx slices per residue
-// class ra (n_full of 512 columns, then possibly the remainder); pairs past
-// ksplit * n_fullx serve a narrow remainder slice (rem <= 256 columns, next to
-// full slices) for residues ra and rb = ra + 1 (rb = -1: none).
+// class ra (n_full of cw columns, then possibly the remainder); pairs past
+// ksplit * n_fullx serve a narrow remainder slice (rem <= cw/2 columns, next
+// to full slices) for residues ra and rb = ra + 1 (rb = -1: none).
 __device__ __forceinline__ void consumer_slice(const Params& p, int c, int& d0, int& nd, int& ra, int& rb) {
   const int n_res = p.ksplit * p.n_fullx;
   if (c < n_res) {
     const int sl = c % p.n_fullx;
     ra = c / p.n_fullx;
     rb = -1;
-    d0 = sl * 512;
-    nd = sl < p.n_full ? 512 : p.rem;
+    d0 = sl * p.cw;
+    nd = sl < p.n_full ? p.cw : p.rem;
   } else {
     const int h = c - n_res;
     ra = 2 * h;
     rb = 2 * h + 1 < p.ksplit ? 2 * h + 1 : -1;
-    d0 = p.n_full * 512;
+    d0 = p.n_full * p.cw;
     nd = p.rem;
   }
 }
@@ -635,6 +639,17 @@ __device__ __forceinline__ void consumer_slice(const Params& p, int c, int& d0, 
 // u-th tile of a consumer pair (ascending; may exceed n_vt, which callers skip).
 __device__ __forceinline__ int consumer_tile(int u, int ra, int rb, int ks) {
   return rb < 0 ? ra + u * ks : (u >> 1) * ks + ((u & 1) ? rb : ra);
+}
+
+__device__ __forceinline__ uint64_t make_policy(int kind) {
+  uint64_t r = 0;
+  if (kind == 1)
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(r));
+  else if (kind == 2)
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(r));
+  else if (kind == 3)
+    asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(r));
+  return r;
 }
 
 __device__ __forceinline__ void pair_load(uint32_t dst, const CUtensorMap* map, int x, int y, uint32_t bar,
@@ -692,7 +707,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int ksteps_d = p.d / kBK;
     if (warp == 0) {
       if (lane == 0 && n_my > 0) {
-        const uint64_t pol = policy_evict_last();
+        const uint64_t pol_h = make_policy(p.pol[0]), pol_e = make_policy(p.pol[1]);
+        const int n_stages = p.ring_bytes / (int)kStageA2;
         int stage = 0;
         uint32_t ph = 0;
         bool ok = true;
@@ -704,9 +720,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t fl = mapa_shared(fb, 0);
             const uint32_t sb = s_base + stage * kStageA2;
             if (leader) mbar_expect_tx(fb, 2 * kStageA2);
-            pair_load(sb, &tm_h, ks * kBK, (int)rank * 128, fl, p.l2hint, pol);
-            pair_load(sb + 16384, &tm_ek, ks * kBK, t * kVT + (int)rank * 128, fl, p.l2hint, pol);
-            if (++stage == kRingA2) { stage = 0; ph ^= 1; }
+            pair_load(sb, &tm_h, ks * kBK, (int)rank * 128, fl, p.pol[0] != 0, pol_h);
+            pair_load(sb + 16384, &tm_ek, ks * kBK, t * kVT + (int)rank * 128, fl, p.pol[1] != 0, pol_e);
+            if (++stage == n_stages) { stage = 0; ph ^= 1; }
           }
         }
       }
@@ -714,6 +730,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp == 1) {
       if (leader && lane == 0 && n_my > 0) {
         const uint32_t idesc = idesc_bf16_f32(256, kVT, 0, 0);
+        const int n_stages = p.ring_bytes / (int)kStageA2;
         int stage = 0;
         uint32_t ph = 0;
         bool ok = true;
@@ -731,7 +748,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               mma_bf16_pair(tmem + b * 256, sdesc_sw128(sb + k * 32, 0, 1024), sdesc_sw128(sb + 16384 + k * 32, 0, 1024),
                             idesc, (ks | k) != 0);
             mma_commit_pair_mc(smem_addr(&bar_empty[stage]), 3);
-            if (++stage == kRingA2) { stage = 0; ph ^= 1; }
+            if (++stage == n_stages) { stage = 0; ph ^= 1; }
           }
           if (ok) mma_commit_pair_mc(smem_addr(&bar_tfull[b]), 3);
         }
@@ -851,14 +868,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int N1 = n_mma == 2 ? (nd - 256 <= 128 ? 128 : 256) : 0;
     const uint32_t e1_off = 16384u + (uint32_t)(N0 / 128) * 8192u;  // E block of the second MMA
     const uint32_t stage_bytes = e1_off + (uint32_t)(N1 / 128) * 8192u;
-    const int n_stages = kRingBytes / (int)stage_bytes < kMaxRing ? kRingBytes / (int)stage_bytes : kMaxRing;
+    const int n_stages = p.ring_bytes / (int)stage_bytes < kMaxRing ? p.ring_bytes / (int)stage_bytes : kMaxRing;
     const int cnt_a = ra < p.n_vt ? (p.n_vt - ra + p.ksplit - 1) / p.ksplit : 0;
     const int cnt_b = rb >= 0 && rb < p.n_vt ? (p.n_vt - rb + p.ksplit - 1) / p.ksplit : 0;
     const int n_iter = rb < 0 ? cnt_a : 2 * cnt_a;
     const int n_my = cnt_a + cnt_b;
     if (warp == 0) {
       if (lane == 0 && n_my > 0) {
-        const uint64_t pol = policy_evict_first();
+        const uint64_t pol_p = make_policy(p.pol[2]), pol_e = make_policy(p.pol[3]);
         int stage = 0;
         uint32_t ph = 0;
         bool ok = true;
@@ -873,13 +890,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t fl = mapa_shared(fb, 0);
             const uint32_t sb = s_base + stage * stage_bytes;
             if (leader) mbar_expect_tx(fb, 2 * stage_bytes);
-            pair_load(sb, &tm_p, 0, ((t * 4 + ks) * 2 + (int)rank) * 128, fl, p.l2hint, pol);
+            pair_load(sb, &tm_p, 0, ((t * 4 + ks) * 2 + (int)rank) * 128, fl, p.pol[2] != 0, pol_p);
             for (int m = 0; m < n_mma; ++m) {
               const int Nm = m ? N1 : N0;
               const uint32_t eb = sb + (m ? e1_off : 16384u);
               for (int bx = 0; bx < Nm / 128; ++bx)
                 pair_load(eb + bx * 8192, &tm_emn, d0 + m * 256 + (int)rank * (Nm / 2) + bx * 64, t * kVT + ks * 64,
-                          fl, p.l2hint, pol);
+                          fl, p.pol[3] != 0, pol_e);
             }
             if (++stage == n_stages) { stage = 0; ph ^= 1; }
           }
@@ -1169,35 +1186,49 @@ int pair_capacity() {
 }
 
 struct PairPlan {
-  int n_vt, n_pa, n_pc, ksplit, n_full, rem, n_fullx;
+  int n_vt, n_pa, n_pc, ksplit, n_full, rem, n_fullx, cw;
 };
 
 // Splits the pairs between the roles and picks the number of vocabulary residue
 // classes (ksplit) that maximises the tile rate, in units of one producer
-// pair's rate: producers give n_pa; a consumer pair of width w finishes a tile
-// in w/d of a producer tile-time, so the residue classes sustain ksplit * d / w
-// (remainder pairs, serving two classes, ksplit * d / (2 rem)). False if no
-// split fits.
+// pair's rate: producers give n_pa; a consumer pair of width w does w/d of a
+// producer pair's work per tile at kConsumerRate of its speed, so the residue
+// classes sustain kConsumerRate * ksplit * d / w (remainder pairs, serving two
+// classes, kConsumerRate * ksplit * d / (2 rem)). False if no split fits.
+//
+// kConsumerRate is measured, not derived: consumers start one producer tile
+// late, receive tiles in bursts and finish after the last one is published.
+// At V = 262144, d = 2816 (512-column slices) the step took 0.597 / 0.536 /
+// 0.598 ms with 37 / 32 / 26 producer pairs, and with 256-column slices
+// 0.651 / 0.536 / 0.704 ms with 43 / 32 / 26; 0.73 makes the plan pick 32.
+constexpr double kConsumerRate = 0.73;
 bool make_pair_plan(int V, int d, PairPlan* q) {
   static const char* single = getenv("DG_VOCAB_SINGLE_SM");
   if (single && single[0] == '1') return false;
   const int pairs = pair_capacity() < num_sms() / 2 ? pair_capacity() : num_sms() / 2;
+  // consumer slice width: 256 columns (one MMA of N = 256 per k-slice); 512
+  // (two MMAs sharing the P operand) measured 0.5-1% slower at d = 2816 and is
+  // kept behind DG_VOCAB_CW=512
+  static const int cw_env = env_int("DG_VOCAB_CW", 256);
+  static const int ks_env = env_int("DG_VOCAB_KSPLIT", 0);
+  q->cw = cw_env == 512 ? 512 : 256;
   q->n_vt = (V + kVT - 1) / kVT;
-  q->n_full = d / 512;
-  q->rem = d % 512;
-  // A remainder of at most 256 columns next to full slices gets pairs that serve
+  q->n_full = d / q->cw;
+  q->rem = d % q->cw;
+  // A remainder of at most cw/2 columns next to full slices gets pairs that serve
   // two residue classes; otherwise the remainder is one more per-class slice.
-  const bool half = q->rem > 0 && q->rem <= 256 && q->n_full > 0;
+  const bool half = q->rem > 0 && q->rem <= q->cw / 2 && q->n_full > 0;
   q->n_fullx = q->n_full + (q->rem > 0 && !half ? 1 : 0);
-  const double wmax = q->n_full > 0 ? 512.0 : (double)q->rem;
+  const double wmax = q->n_full > 0 ? (double)q->cw : (double)q->rem;
   double best = -1.0;
   for (int ks = 1; ks <= 32 && ks <= q->n_vt; ++ks) {
+    if (ks_env && ks != ks_env) continue;
     const int n_pc = ks * q->n_fullx + (half ? (ks + 1) / 2 : 0);
     if (n_pc >= pairs) break;
     const int n_pa = pairs - n_pc < q->n_vt ? pairs - n_pc : q->n_vt;
     double cons = 1e30;
-    if (q->n_fullx > 0) cons = fmin(cons, ks * (double)d / wmax);
-    if (half) cons = fmin(cons, ks * (double)d / (2.0 * q->rem));
+    if (q->n_fullx > 0) cons = fmin(cons, kConsumerRate * ks * (double)d / wmax);
+    if (half) cons = fmin(cons, kConsumerRate * ks * (double)d / (2.0 * q->rem));
     const double rate = fmin((double)n_pa, cons);
     if (rate > best + 1e-9) {
       best = rate;
@@ -1282,10 +1313,19 @@ int vocab_tc_launch(const __nv_bfloat16* h, const __nv_bfloat16* emb, int C, int
   p.n_full = pairs ? pq.n_full : 0;
   p.rem = pairs ? pq.rem : 0;
   p.n_fullx = pairs ? pq.n_fullx : 0;
+  p.cw = pairs ? pq.cw : 0;
+  p.ring_bytes = kRingBytes;
   // L2 eviction hints on by default (measured: DRAM reads 725 -> 601 MB at
   // V=65536); DG_VOCAB_L2HINT=2 turns them off for comparison.
   static const int l2hint = env_int("DG_VOCAB_L2HINT", 1);
   p.l2hint = l2hint == 1;
+  // paired form: H and producer E evict_last, P and consumer E evict_first
+  // (DG_VOCAB_L2POL=dddd overrides, one digit per stream as in Params::pol)
+  static const char* pol_env = getenv("DG_VOCAB_L2POL");
+  for (int k = 0; k < 4; ++k) {
+    const int dflt = l2hint == 1 ? (k < 2 ? 1 : 2) : 0;
+    p.pol[k] = pol_env && strlen(pol_env) == 4 && pol_env[k] >= '0' && pol_env[k] <= '3' ? pol_env[k] - '0' : dflt;
+  }
   int* flags = (int*)(w + L.flags);
   p.ready = flags;
   p.consumed = flags + pl.n_vt;
@@ -1312,7 +1352,7 @@ int vocab_tc_launch(const __nv_bfloat16* h, const __nv_bfloat16* emb, int C, int
   DG_CUDA_TRY(cudaMemsetAsync(flags, 0, L.flag_bytes, s));
 
   if (pairs) {
-    const size_t psmem = (size_t)kRingBytes + 1024;  // attribute set by pair_capacity()
+    const size_t psmem = (size_t)p.ring_bytes + 1024;  // attribute (the maximum) set by pair_capacity()
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(2 * (pq.n_pa + pq.n_pc));
     cfg.blockDim = dim3(kThreads);
@@ -1325,8 +1365,11 @@ int vocab_tc_launch(const __nv_bfloat16* h, const __nv_bfloat16* emb, int C, int
     attr[1].val.clusterDim.x = 2;
     attr[1].val.clusterDim.y = 1;
     attr[1].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 2;
+    // DG_VOCAB_NONCOOP=1 drops the cooperative attribute (for profilers that
+    // cannot co-schedule it; every cross-CTA wait is bounded either way)
+    static const int noncoop = env_int("DG_VOCAB_NONCOOP", 0);
+    cfg.attrs = noncoop == 1 ? attr + 1 : attr;
+    cfg.numAttrs = noncoop == 1 ? 1 : 2;
     DG_CUDA_TRY(cudaLaunchKernelEx(&cfg, vocab_pair, tm_h, tm_ek, tm_emn, tm_p, p));
   } else {
   const size_t smem = (size_t)kStages * kStageBytes + 1024;

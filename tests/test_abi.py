@@ -108,8 +108,8 @@ def test_vocab_plan_is_a_host_query(lib):
     n_a, n_c, ks, pair, grid, n_vt = list(buf)
     assert n_vt == 1024 and n_a + n_c == grid
     if pair:
-        # CTA pairs: 2816 = 5 slices of 512 + 256; the 256-wide slice's pairs serve two residue classes
-        assert n_a % 2 == 0 and n_c == 2 * (5 * ks + (ks + 1) // 2) and grid <= 152
+        # CTA pairs: consumers own 256-column slices, 2816 = 11 of them per residue class
+        assert n_a % 2 == 0 and n_c == 2 * 11 * ks and grid <= 152
     else:
         assert n_c % 11 == 0 and n_c // 11 == ks
     assert lib.dg_vocab_step_plan(256, 262144, 2800, B.DG_BF16, ctypes.cast(buf, ctypes.c_void_p)) == B.DG_ERR_INVALID_ARG
