@@ -313,11 +313,11 @@ def run_graphed_blocks(args, world, rank, local, w, dev, seed):
                    "blocks": w.blocks, "steps_per_canvas": w.steps, "threshold": w.thresholds[0], "alpha": w.alpha,
                    "parallelism": f"replicas{world}", "cuda_graph": "one per canvas, device-side cache length",
                    "l2": "inputs larger than L2 (embedding table %.2f GB), no flush" % (w.V * w.d * 2 / 1e9)},
-        "roofline": {"kernel": "dg_vocab_step_renoise_devpos (vocab_main + vocab_combine)", "bound": "tensor",
+        "roofline": {"kernel": f"dg_vocab_step_renoise_devpos ({vocab_kernel(w)} + vocab_combine)", "bound": "tensor",
                      "achieved": round(flops / (vocab_ms / 1e3) / 1e12, 1), "peak": pk["bf16_tflops"],
                      "unit": "TFLOP/s", "frac": round(flops / (vocab_ms / 1e3) / 1e12 / pk["bf16_tflops"], 4),
                      # same vocabulary-step shapes as the headline workload, so its capture applies
-                     "traffic": committed_traffic("vocab_main", "v262k_d2816_p4k"),
+                     "traffic": committed_traffic(vocab_kernel(w), "v262k_d2816_p4k"),
                      "peak_source": f"{pk['source']} bf16 burst",
                      "algorithmic_flops_per_launch": flops, "avg_launch_ms": round(vocab_ms, 4)},
         "roofline_attention": {"kernel": f"dg_canvas_attn_devlen (attn_fwd_tc) at prefix {P_last}", "bound": "tensor",
@@ -484,8 +484,8 @@ def run_ours(args, world, rank, local):
     pk = peaks()
     flops = 4.0 * w.C * w.V * w.d
     achieved = flops / (vocab_ms / 1e3) / 1e12
-    traffic = committed_traffic("vocab_main", args.workload)
-    roof = {"kernel": "dg_vocab_step_renoise (vocab_main + vocab_combine)", "bound": "tensor",
+    traffic = committed_traffic(vocab_kernel(w), args.workload)
+    roof = {"kernel": f"dg_vocab_step_renoise ({vocab_kernel(w)} + vocab_combine)", "bound": "tensor",
             "achieved": round(achieved, 1), "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
             "frac": round(achieved / pk["bf16_tflops"], 4), "traffic": traffic,
             "peak_source": f"{pk['source']} bf16 burst", "algorithmic_flops_per_launch": flops,
@@ -548,6 +548,13 @@ def capture_canvas_graph(cv, stream, spc):
         g.replay()  # one untimed replay
     stream.synchronize()
     return g, n
+
+
+def vocab_kernel(w):
+    """Name of the vocabulary step's main kernel in the library's launch plan:
+    vocab_pair (CTA pairs) where two-CTA clusters fit, else vocab_main."""
+    from canvas_denoising_gb300 import binding as B
+    return "vocab_pair" if B.vocab_step_plan(w.C, w.V, w.d)["cluster_pairs"] else "vocab_main"
 
 
 def committed_traffic(kernel, workload):

@@ -12,24 +12,30 @@
 //    every P tile exp(l - R_i) is final the moment its logits exist: P.E
 //    and the row sums accumulate linearly in any order, with no rescaling
 //    of accumulators. R_i is the maximum over a sample of the vocabulary
-//    (every producer CTA's first tile, agreed on through one grid-wide
-//    count). A row whose true maximum exceeds R_i + 40 (exp would leave the
-//    safe fp32 range) is flagged and recomputed exactly by the combine
-//    kernel with R = its true maximum.
-//  * Two CTA roles, one CTA per SM, all co-resident (cooperative launch):
-//    - producer ("A") CTAs own vocabulary tiles of 128 ids (round robin).
-//      GEMM1: logits[rows x 128] = H . E_tile^T, K-loop over d in steps of
-//      64 through a 4-stage TMA ring, two M=128 MMAs per k-step (row halves)
-//      into a double-buffered TMEM accumulator. Four epilogue warps read the
-//      logits from TMEM, keep per-row running max / first argmax / sum of
-//      exp(l - R), and write P = exp(l - R) in bf16 to a global ring,
-//      already in the 128-byte-swizzled K-major layout an MMA operand needs,
-//      then publish the tile with a release flag.
-//    - consumer ("C") CTAs own a [128 rows x 256 d] slice of S and a residue
-//      class of vocabulary tiles. GEMM2: S_slice += P_tile . E_tile[:, slice]
-//      with E read MN-major (the same rows the producer just streamed, so
-//      from L2), accumulating in TMEM over the whole vocabulary. Their fp32
-//      partials go to the workspace once, at the end.
+//    (every producer's first tile, agreed on through one grid-wide count).
+//    A row whose true maximum exceeds R_i + 40 (exp would leave the safe
+//    fp32 range) is flagged and recomputed exactly by the combine kernel
+//    with R = its true maximum.
+//  * Two roles, all co-resident (cooperative launch, one CTA per SM):
+//    - producers own vocabulary tiles of 256 ids (round robin). GEMM1:
+//      logits[rows x 256] = H . E_tile^T, K-loop over d in steps of 64
+//      through a TMA ring. Eight epilogue warps read the logits from TMEM,
+//      keep per-row running max / first argmax / sum of exp(l - R), and
+//      write P = exp(l - R) in bf16 to a global ring, already in the
+//      128-byte-swizzled K-major layout an MMA operand needs, then publish
+//      the tile with a release flag.
+//    - consumers own a slice of S's columns and a residue class of
+//      vocabulary tiles. GEMM2: S_slice += P_tile . E_tile[:, slice] with E
+//      read MN-major (the rows producers just streamed, mostly from L2),
+//      accumulating in TMEM over the whole vocabulary. Their fp32 partials
+//      go to the workspace once, at the end.
+//  * Two forms of those roles:
+//    - vocab_pair (default): CTA pairs (clusters of two, cta_group::2). One
+//      MMA of M = 256 spans the pair, so each SM reads half of the wide
+//      operand from shared memory and holds 128 rows of the accumulator;
+//      the producer accumulator is double-buffered in TMEM.
+//    - vocab_main: one CTA per role unit (cta_group::1), M = 128 MMAs for
+//      each row half; used where two-CTA clusters cannot be placed.
 //  * A combine kernel merges producer statistics (max, lowest argmax, sums)
 //    and consumer partials into argmax, conf, lse and S (bf16).
 // Every wait is bounded (about two seconds of clock); on expiry the kernel
