@@ -326,6 +326,9 @@ def run_graphed_blocks(args, world, rank, local, w, dev, seed):
                                "frac": round(aflops / (attn_ms / 1e3) / 1e12 / pk["bf16_tflops"], 4),
                                "traffic": None, "algorithmic_flops_per_launch": aflops,
                                "avg_launch_ms": round(attn_ms, 4)},
+        # attention at the mean prefix over the canvases (prefix + b*C for canvas b)
+        "roofline_step": step_roofline(flops + 4.0 * w.C * (w.prefix + (w.blocks - 1) * w.C / 2 + w.C) * w.hd * w.Hq,
+                                       ms / K, pk),
         "gpu_launches": replays * gb.launches * world, "cuda_graph": True, "clocks": clk, "device_status": status,
         "e2e": None,
     }
@@ -415,6 +418,37 @@ def run_ours(args, world, rank, local):
         selfcond=cv.selfcond, renoised=cv.renoised, workspace=cv.ws_vocab, stream=stream), 20)
     attn_ms = per_call(lambda i: B.canvas_attn(q0, cv.k, cv.v, cv.P, kn0, vn0, out=cv.out, lse=cv.lse_attn,
                                                workspace=cv.ws_attn, stream=stream), 50)
+
+    # Workloads whose operands fit in L2 (the 32k-vocabulary one: E is 64 MiB) run warm above; the same
+    # calls and whole steps are also timed with L2 flushed before each one (a 256 MiB write), events
+    # around the call only.
+    flushed = None
+    if fits_in_l2(w):
+        flush_buf = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+
+        def per_call_flushed(fn, n):
+            pairs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                     for _ in range(n)]
+            with torch.cuda.stream(stream):
+                fn(0)
+                torch.cuda._sleep(20_000_000)
+                for i in range(n):
+                    flush_buf.fill_(i & 0xFF)
+                    pairs[i][0].record(stream)
+                    fn(i)
+                    pairs[i][1].record(stream)
+            stream.synchronize()
+            return sum(a.elapsed_time(b) for a, b in pairs) / n
+
+        flushed = {
+            "vocab_ms": per_call_flushed(lambda i: B.vocab_step_renoise(
+                h0, cv.emb, cv.tokens, w.thresholds[0], cv.seed, i, cv.P, argmax=cv.argmax, conf=cv.conf,
+                lse=cv.lse, selfcond=cv.selfcond, renoised=cv.renoised, workspace=cv.ws_vocab, stream=stream), 20),
+            "attn_ms": per_call_flushed(lambda i: B.canvas_attn(q0, cv.k, cv.v, cv.P, kn0, vn0, out=cv.out,
+                                                                lse=cv.lse_attn, workspace=cv.ws_attn,
+                                                                stream=stream), 20),
+            "step_ms": per_call_flushed(lambda i: cv.step(i, stream), 2 * w.steps),
+        }
 
     # ---- end to end through the public API: per-step inputs from pinned host memory, result back.
     # As a pipelined caller would: the next step's inputs are copied on a second stream into the
@@ -513,7 +547,7 @@ def run_ours(args, world, rank, local):
         "config": {"workload": w.name, "canvas": w.C, "vocab": w.V, "d_model": w.d, "q_heads": w.Hq,
                    "kv_heads": w.Hkv, "head_dim": w.hd, "kv_prefix": w.prefix, "threshold": w.thresholds[0],
                    "steps_per_canvas": w.steps, "alpha": w.alpha, "parallelism": f"replicas{world}",
-                   "l2": "inputs larger than L2 (embedding table %.2f GB), no flush" % (w.V * w.d * 2 / 1e9)},
+                   "l2": l2_label(w)},
         "roofline": roof,
         "roofline_attention": roof_attn,
         "gpu_launches": launches * world,
@@ -522,6 +556,16 @@ def run_ours(args, world, rank, local):
     }
     if e2e is not None:
         line["e2e"] = e2e
+    line["roofline_step"] = step_roofline(flops + aflops, ms / K, pk)
+    if flushed is not None:
+        fl_steps = job_rate(world, 1, flushed["step_ms"])
+        line["l2_flushed"] = {
+            "value": round(fl_steps, 3), "unit": "steps/s", "ms_per_step": round(flushed["step_ms"], 5),
+            "vocab_ms": round(flushed["vocab_ms"], 4),
+            "vocab_frac": round(flops / (flushed["vocab_ms"] / 1e3) / 1e12 / pk["bf16_tflops"], 4),
+            "attn_ms": round(flushed["attn_ms"], 4),
+            "attn_frac": round(aflops / (flushed["attn_ms"] / 1e3) / 1e12 / pk["bf16_tflops"], 4),
+            "timing": "each call / eager step after a 256 MiB write that evicts L2; events around the call only"}
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, cv)
     if world > 1:
@@ -548,6 +592,34 @@ def capture_canvas_graph(cv, stream, spc):
         g.replay()  # one untimed replay
     stream.synchronize()
     return g, n
+
+
+def step_roofline(step_flops, ms_per_step, pk):
+    """The whole step against the bf16 peak: the step's algorithmic FLOPs (vocabulary step + attention)
+    over the measured time per step (the timed region, graph replays)."""
+    ach = step_flops / (ms_per_step / 1e3) / 1e12
+    out = {"bound": "tensor", "achieved": round(ach, 1), "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
+           "frac": round(ach / pk["bf16_tflops"], 4), "algorithmic_flops_per_step": step_flops}
+    if pk.get("bf16_tflops_sustained"):
+        out["frac_sustained"] = round(ach / pk["bf16_tflops_sustained"], 4)
+    return out
+
+
+L2_BYTES = 126 * 2**20  # this GPU's L2 (129 MB nominal, ~126 MiB usable)
+
+
+def fits_in_l2(w):
+    """True if the step's large operands (E, the K/V cache) fit in L2 together."""
+    el = 2 if w.dtype == "bf16" else 4
+    return w.V * w.d * el + 2 * w.Hkv * w.cap * w.hd * el < L2_BYTES
+
+
+def l2_label(w):
+    gb = w.V * w.d * (2 if w.dtype == "bf16" else 4) / 1e9
+    if fits_in_l2(w):
+        return ("operands fit in L2 (embedding table %.3f GB): steps/s and roofline per-call times with L2 warm; "
+                "the same after an L2 flush in l2_flushed" % gb)
+    return "inputs larger than L2 (embedding table %.2f GB), no flush" % gb
 
 
 def vocab_kernel(w):
