@@ -138,7 +138,7 @@ Layout make_layout(const Plan& p, int d) {
   Layout L;
   size_t o = 0;
   L.flags = o;
-  L.flag_bytes = (size_t)(2 * p.n_vt + 2 + 256) * sizeof(int);
+  L.flag_bytes = (size_t)(2 * p.n_vt + 2 + 256 + 256) * sizeof(int);  // + per-row reference keys
   o += up256(L.flag_bytes);
   L.smax = o; o += up256((size_t)p.n_a * 256 * 4);
   L.am = o;   o += up256((size_t)p.n_a * 256 * 4);
@@ -158,6 +158,7 @@ struct Params {
   int* ref_count;  // producers that have published their sample maxima
   int* abort_flag;
   int* overflow;   // [256]
+  unsigned* rowkey;  // [256] paired form: running max of the sample, order-preserving key (0 = none)
   float* smax;     // [256][n_a] sample maxima
   float* am;       // [256][n_a] running max
   int* aa;         // [256][n_a] first argmax
@@ -177,7 +178,7 @@ struct Params {
   int* status;
   // paired form only: producer pairs, and the consumer pairs' d-slicing
   // (n_full slices of 512 columns, then a remainder of `rem` columns; see consumer_slice)
-  int n_pa, n_full, rem, n_fullx, cw;
+  int n_pa, n_pc, n_full, rem, n_fullx, cw;
   // paired form: L2 policy per operand stream (H, producer E, P, consumer E):
   // 0 none, 1 evict_last, 2 evict_first, 3 evict_normal
   int pol[4];
@@ -642,6 +643,25 @@ __device__ __forceinline__ void consumer_slice(const Params& p, int c, int& d0, 
   }
 }
 
+// Order-preserving map of fp32 to uint32 (larger float -> larger key; every
+// key of a float is above 0, the key the workspace starts from).
+__device__ __forceinline__ unsigned order_key(float x) {
+  const unsigned b = __float_as_uint(x);
+  return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+__device__ __forceinline__ float from_order_key(unsigned k) {
+  return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
+}
+__device__ __forceinline__ void red_max_u32(unsigned* a, unsigned v) {
+  asm volatile("red.relaxed.gpu.global.max.u32 [%0], %1;" ::"l"(a), "r"(v) : "memory");
+}
+
+// j-th tile a pair produces: its own index first (every pair takes part in the
+// first round), then, for producer pairs, every n_pa-th tile after the first round.
+__device__ __forceinline__ int prod_tile(const Params& p, int pair, int j) {
+  return j == 0 ? pair : p.n_pa + p.n_pc + pair + (j - 1) * p.n_pa;
+}
+
 // u-th tile of a consumer pair (ascending; may exceed n_vt, which callers skip).
 __device__ __forceinline__ int consumer_tile(int u, int ra, int rb, int ks) {
   return rb < 0 ? ra + u * ks : (u >> 1) * ks + ((u & 1) ? rb : ra);
@@ -670,7 +690,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     vocab_pair(const __grid_constant__ CUtensorMap tm_h, const __grid_constant__ CUtensorMap tm_ek,
                const __grid_constant__ CUtensorMap tm_emn, const __grid_constant__ CUtensorMap tm_p, const Params p) {
   extern __shared__ __align__(1024) uint8_t smem_dyn[];
-  __shared__ __align__(8) uint64_t bar_full[kMaxRing], bar_empty[kMaxRing], bar_tfull[2], bar_tempty[2], bar_drain;
+  // ring barriers of the produce phase (full/empty) and of the consume phase (full2/empty2)
+  __shared__ __align__(8) uint64_t bar_full[kMaxRing], bar_empty[kMaxRing], bar_full2[kMaxRing], bar_empty2[kMaxRing];
+  __shared__ __align__(8) uint64_t bar_tfull[2], bar_tempty[2], bar_drain;
   __shared__ uint32_t tmem_slot;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -685,6 +707,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int s = 0; s < kMaxRing; ++s) {
       mbar_init(smem_addr(&bar_full[s]), 1);
       mbar_init(smem_addr(&bar_empty[s]), 1);
+      mbar_init(smem_addr(&bar_full2[s]), 1);
+      mbar_init(smem_addr(&bar_empty2[s]), 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(smem_addr(&bar_tfull[b]), 1);
@@ -706,20 +730,38 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = tmem_slot;
 
-  if (is_a) {
-    // ===================================================== producer pair: GEMM1 + softmax epilogue
-    const int a = pair;
-    const int n_my = a < p.n_vt ? (p.n_vt - a + p.n_pa - 1) / p.n_pa : 0;
-    const int ksteps_d = p.d / kBK;
-    if (warp == 0) {
-      if (lane == 0 && n_my > 0) {
+  const int NP = p.n_pa + p.n_pc;
+  const int ksteps_d = p.d / kBK;
+  const int n_stages_a = p.ring_bytes / (int)kStageA2;
+  // Produce phase (every pair): a pair's first tile is its pair index, so the
+  // first round covers NP tiles while nothing has been published for the
+  // consumers yet; producer pairs then continue with NP + pair + (j-1)*n_pa.
+  int n_prod = pair < p.n_vt ? 1 : 0;
+  if (is_a && NP + pair < p.n_vt) n_prod += (p.n_vt - NP - pair + p.n_pa - 1) / p.n_pa;
+  // Consume phase (consumer pairs): a d-slice and residue class(es) of tiles.
+  int d0 = 0, nd = 256, ra = 0, rb = -1;
+  if (!is_a) consumer_slice(p, pair - p.n_pa, d0, nd, ra, rb);
+  const int n_mma = nd > 256 ? 2 : 1;
+  const int N0 = nd >= 256 ? 256 : (nd <= 128 ? 128 : 256);
+  const int N1 = n_mma == 2 ? (nd - 256 <= 128 ? 128 : 256) : 0;
+  const uint32_t e1_off = 16384u + (uint32_t)(N0 / 128) * 8192u;  // E block of the second MMA
+  const uint32_t stage_c = e1_off + (uint32_t)(N1 / 128) * 8192u;
+  const int n_stages_c = p.ring_bytes / (int)stage_c < kMaxRing ? p.ring_bytes / (int)stage_c : kMaxRing;
+  const int cnt_a = !is_a && ra < p.n_vt ? (p.n_vt - ra + p.ksplit - 1) / p.ksplit : 0;
+  const int cnt_b = !is_a && rb >= 0 && rb < p.n_vt ? (p.n_vt - rb + p.ksplit - 1) / p.ksplit : 0;
+  const int n_iter = rb < 0 ? cnt_a : 2 * cnt_a;
+  const int n_cons = cnt_a + cnt_b;
+
+  if (warp == 0) {
+    // ===================================================== TMA issue (both CTAs)
+    if (lane == 0) {
+      bool ok = true;
+      if (n_prod > 0) {
         const uint64_t pol_h = make_policy(p.pol[0]), pol_e = make_policy(p.pol[1]);
-        const int n_stages = p.ring_bytes / (int)kStageA2;
         int stage = 0;
         uint32_t ph = 0;
-        bool ok = true;
-        for (int j = 0; j < n_my && ok; ++j) {
-          const int t = a + j * p.n_pa;
+        for (int j = 0; j < n_prod && ok; ++j) {
+          const int t = prod_tile(p, pair, j);
           for (int ks = 0; ks < ksteps_d; ++ks) {
             if (!wait_bar(smem_addr(&bar_empty[stage]), ph ^ 1, p)) { ok = false; break; }
             const uint32_t fb = smem_addr(&bar_full[stage]);
@@ -728,22 +770,54 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (leader) mbar_expect_tx(fb, 2 * kStageA2);
             pair_load(sb, &tm_h, ks * kBK, (int)rank * 128, fl, p.pol[0] != 0, pol_h);
             pair_load(sb + 16384, &tm_ek, ks * kBK, t * kVT + (int)rank * 128, fl, p.pol[1] != 0, pol_e);
-            if (++stage == n_stages) { stage = 0; ph ^= 1; }
+            if (++stage == n_stages_a) { stage = 0; ph ^= 1; }
           }
         }
       }
-      __syncwarp();
-    } else if (warp == 1) {
-      if (leader && lane == 0 && n_my > 0) {
-        const uint32_t idesc = idesc_bf16_f32(256, kVT, 0, 0);
-        const int n_stages = p.ring_bytes / (int)kStageA2;
+      if (ok && n_cons > 0) {
+        // the ring is reused with its own barriers: the produce phase's MMAs must have read it
+        if (n_prod > 0 && !wait_bar(smem_addr(&bar_tfull[0]), 0, p)) ok = false;
+        const uint64_t pol_p = make_policy(p.pol[2]), pol_e = make_policy(p.pol[3]);
         int stage = 0;
         uint32_t ph = 0;
-        bool ok = true;
-        for (int j = 0; j < n_my && ok; ++j) {
+        for (int u = 0; u < n_iter && ok; ++u) {
+          const int t = consumer_tile(u, ra, rb, p.ksplit);
+          if (t >= p.n_vt) continue;
+          if (!wait_flag(p.ready + t, 2, p)) break;
+          fence_proxy_async_global();
+          for (int ks = 0; ks < kVT / 64; ++ks) {
+            if (!wait_bar(smem_addr(&bar_empty2[stage]), ph ^ 1, p)) { ok = false; break; }
+            const uint32_t fb = smem_addr(&bar_full2[stage]);
+            const uint32_t fl = mapa_shared(fb, 0);
+            const uint32_t sb = s_base + stage * stage_c;
+            if (leader) mbar_expect_tx(fb, 2 * stage_c);
+            pair_load(sb, &tm_p, 0, ((t * 4 + ks) * 2 + (int)rank) * 128, fl, p.pol[2] != 0, pol_p);
+            for (int m = 0; m < n_mma; ++m) {
+              const int Nm = m ? N1 : N0;
+              const uint32_t eb = sb + (m ? e1_off : 16384u);
+              for (int bx = 0; bx < Nm / 128; ++bx)
+                pair_load(eb + bx * 8192, &tm_emn, d0 + m * 256 + (int)rank * (Nm / 2) + bx * 64, t * kVT + ks * 64,
+                          fl, p.pol[3] != 0, pol_e);
+            }
+            if (++stage == n_stages_c) { stage = 0; ph ^= 1; }
+          }
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ===================================================== MMA issue (even CTA)
+    if (leader && lane == 0) {
+      bool ok = true;
+      if (n_prod > 0) {
+        // GEMM1: logits of a tile into accumulator j & 1 (128 rows x 256 ids per CTA)
+        const uint32_t idesc = idesc_bf16_f32(256, kVT, 0, 0);
+        int stage = 0;
+        uint32_t ph = 0;
+        for (int j = 0; j < n_prod && ok; ++j) {
           const int b = j & 1;
           // accumulator b must have been read out (tile j-2) by both CTAs' epilogues
-          if (!wait_bar(smem_addr(&bar_tempty[b]), ((uint32_t)(j >> 1) & 1u) ^ 1u, p)) break;
+          if (!wait_bar(smem_addr(&bar_tempty[b]), ((uint32_t)(j >> 1) & 1u) ^ 1u, p)) { ok = false; break; }
           tc_fence_after();
           for (int ks = 0; ks < ksteps_d; ++ks) {
             if (!wait_bar(smem_addr(&bar_full[stage]), ph, p)) { ok = false; break; }
@@ -754,175 +828,28 @@ __global__ void __launch_bounds__(kThreads, 1)
               mma_bf16_pair(tmem + b * 256, sdesc_sw128(sb + k * 32, 0, 1024), sdesc_sw128(sb + 16384 + k * 32, 0, 1024),
                             idesc, (ks | k) != 0);
             mma_commit_pair_mc(smem_addr(&bar_empty[stage]), 3);
-            if (++stage == n_stages) { stage = 0; ph ^= 1; }
+            if (++stage == n_stages_a) { stage = 0; ph ^= 1; }
           }
           if (ok) mma_commit_pair_mc(smem_addr(&bar_tfull[b]), 3);
         }
-        mma_commit_pair_mc(smem_addr(&bar_drain), 1);
-        drain_bar(smem_addr(&bar_drain), 0, p);
       }
-      __syncwarp();
-    } else {
-      // epilogue warps 2..9: id half hc of the tile, TMEM lane quarter q
-      const int hc = (warp - 2) >> 2;
-      const int q = warp & 3;
-      const int r = q * 32 + lane;  // row within this CTA's half = TMEM lane
-      const int i = (int)rank * 128 + r;
-      const int slot = a * 2 + hc;
-      const uint32_t tl = tmem + ((uint32_t)(q * 32) << 16) + hc * 128;
-      float R2 = 0.f, lim2 = 0.f;
-      float m_run = -INFINITY, z_run = 0.f;
-      int a_run = 0x7fffffff;
-      bool ovf = false;
-      bool ok = true;
-      if (n_my == 0) {
-        p.smax[(size_t)i * p.n_a + slot] = -INFINITY;
-        __threadfence();
-        epi_sync();
-        if (threadIdx.x == 64) red_release_add_gpu(p.ref_count, 1);
-      }
-      for (int j = 0; j < n_my && ok; ++j) {
-        const int t = a + j * p.n_pa;
-        const int b = j & 1;
-        const bool got = wait_bar(smem_addr(&bar_tfull[b]), (uint32_t)(j >> 1) & 1u, p);
-        if (epi_any(!got)) { ok = false; break; }
+      if (ok && n_cons > 0) {
+        // GEMM2: S_slice += P . E into accumulators at columns 0 (and 256), over buffer 0 of the
+        // produce phase: both CTAs' epilogues must have read that tile's logits
+        if (n_prod > 0 && !wait_bar(smem_addr(&bar_tempty[0]), 0, p)) ok = false;
         tc_fence_after();
-        float v[128];
-        tmem_ld128(tl + b * 256, v);
-        // every logit of this half-tile is in registers: hand the buffer back
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_addr(&bar_tempty[b]), 0));
-        const int vb = t * kVT + hc * 128;
-        if (vb + 128 > p.V) {
-#pragma unroll
-          for (int e = 0; e < 128; ++e)
-            if (vb + e >= p.V) v[e] = -INFINITY;
-        }
-        float bm[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) bm[e] = fmaxf(v[e], v[120 + e]);
-#pragma unroll
-        for (int bb = 8; bb < 120; bb += 16)
-#pragma unroll
-          for (int e = 0; e < 8; ++e) bm[e] = max3(bm[e], v[bb + e], v[bb + 8 + e]);
-        const float cm = max3(max3(bm[0], bm[1], bm[2]), max3(bm[3], bm[4], bm[5]), fmaxf(bm[6], bm[7]));
-        if (j == 0) {
-          // this slot's first half-tile is its sample -> grid-wide reference
-          p.smax[(size_t)i * p.n_a + slot] = cm;
-          __threadfence();
-          epi_sync();
-          if (threadIdx.x == 64) red_release_add_gpu(p.ref_count, 1);
-          const bool refd = wait_flag(p.ref_count, 2 * p.n_pa, p);
-          if (epi_any(!refd)) { ok = false; break; }
-          float R = -INFINITY;
-          const float* sm_row = p.smax + (size_t)i * p.n_a;
-          for (int aa = 0; aa < p.n_a; ++aa) R = fmaxf(R, __ldcg(sm_row + aa));
-          R2 = R * kLog2e;
-          lim2 = (R + kTau) * kLog2e;
-        }
-        if (cm > m_run) {
-          int ci = 127;
-#pragma unroll
-          for (int e = 127; e >= 0; --e)
-            if (v[e] == cm) ci = e;
-          m_run = cm;
-          a_run = vb + ci;
-        }
-        if (cm * kLog2e > lim2) ovf = true;
-        float zs[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) zs[e] = 0.f;
-        // P blocks [t][sub-tile of 64 ids][row half = rank], pre-swizzled K-major
-        uint8_t* prow = p.pbuf + ((size_t)((t * 4 + hc * 2) * 2 + (int)rank)) * kTileBytes + (size_t)r * 128;
-#pragma unroll
-        for (int e8 = 0; e8 < 16; ++e8) {
-          float pe[8];
-#pragma unroll
-          for (int f = 0; f < 8; f += 2) {
-            float x0, x1;
-            fma2(x0, x1, v[e8 * 8 + f], v[e8 * 8 + f + 1], kLog2e, kLog2e, -R2, -R2);
-            pe[f] = ex2_approx(x0);  // masked ids: exp2(-inf) = 0
-            pe[f + 1] = ex2_approx(x1);
-            add2(zs[f], zs[f + 1], pe[f], pe[f + 1]);
-          }
-          const int sub = e8 >> 3, piece = e8 & 7;
-          uint8_t* dst = prow + (size_t)sub * 2 * kTileBytes + ((piece ^ (r & 7)) << 4);
-          *reinterpret_cast<uint4*>(dst) =
-              make_uint4(pack2(pe[0], pe[1]), pack2(pe[2], pe[3]), pack2(pe[4], pe[5]), pack2(pe[6], pe[7]));
-        }
-        z_run += ((zs[0] + zs[1]) + (zs[2] + zs[3])) + ((zs[4] + zs[5]) + (zs[6] + zs[7]));
-        // publish this CTA's half of the P tile (consumers wait for both halves)
-        fence_proxy_async_global();
-        __threadfence();
-        epi_sync();
-        if (threadIdx.x == 64 && !(p.inject && t == 0)) red_release_add_gpu(p.ready + t, 1);
-      }
-      if (i < p.C) {
-        p.am[(size_t)i * p.n_a + slot] = m_run;
-        p.aa[(size_t)i * p.n_a + slot] = a_run;
-        p.az[(size_t)i * p.n_a + slot] = z_run;
-        if (ovf) p.overflow[i] = 1;
-      }
-    }
-  } else {
-    // ===================================================== consumer pair: GEMM2 (S += P . E)
-    int d0, nd, ra, rb;
-    consumer_slice(p, pair - p.n_pa, d0, nd, ra, rb);
-    const int n_mma = nd > 256 ? 2 : 1;
-    const int N0 = nd >= 256 ? 256 : (nd <= 128 ? 128 : 256);
-    const int N1 = n_mma == 2 ? (nd - 256 <= 128 ? 128 : 256) : 0;
-    const uint32_t e1_off = 16384u + (uint32_t)(N0 / 128) * 8192u;  // E block of the second MMA
-    const uint32_t stage_bytes = e1_off + (uint32_t)(N1 / 128) * 8192u;
-    const int n_stages = p.ring_bytes / (int)stage_bytes < kMaxRing ? p.ring_bytes / (int)stage_bytes : kMaxRing;
-    const int cnt_a = ra < p.n_vt ? (p.n_vt - ra + p.ksplit - 1) / p.ksplit : 0;
-    const int cnt_b = rb >= 0 && rb < p.n_vt ? (p.n_vt - rb + p.ksplit - 1) / p.ksplit : 0;
-    const int n_iter = rb < 0 ? cnt_a : 2 * cnt_a;
-    const int n_my = cnt_a + cnt_b;
-    if (warp == 0) {
-      if (lane == 0 && n_my > 0) {
-        const uint64_t pol_p = make_policy(p.pol[2]), pol_e = make_policy(p.pol[3]);
-        int stage = 0;
-        uint32_t ph = 0;
-        bool ok = true;
-        for (int u = 0; u < n_iter && ok; ++u) {
-          const int t = consumer_tile(u, ra, rb, p.ksplit);
-          if (t >= p.n_vt) continue;
-          if (!wait_flag(p.ready + t, 2, p)) break;
-          fence_proxy_async_global();
-          for (int ks = 0; ks < kVT / 64; ++ks) {
-            if (!wait_bar(smem_addr(&bar_empty[stage]), ph ^ 1, p)) { ok = false; break; }
-            const uint32_t fb = smem_addr(&bar_full[stage]);
-            const uint32_t fl = mapa_shared(fb, 0);
-            const uint32_t sb = s_base + stage * stage_bytes;
-            if (leader) mbar_expect_tx(fb, 2 * stage_bytes);
-            pair_load(sb, &tm_p, 0, ((t * 4 + ks) * 2 + (int)rank) * 128, fl, p.pol[2] != 0, pol_p);
-            for (int m = 0; m < n_mma; ++m) {
-              const int Nm = m ? N1 : N0;
-              const uint32_t eb = sb + (m ? e1_off : 16384u);
-              for (int bx = 0; bx < Nm / 128; ++bx)
-                pair_load(eb + bx * 8192, &tm_emn, d0 + m * 256 + (int)rank * (Nm / 2) + bx * 64, t * kVT + ks * 64,
-                          fl, p.pol[3] != 0, pol_e);
-            }
-            if (++stage == n_stages) { stage = 0; ph ^= 1; }
-          }
-        }
-      }
-      __syncwarp();
-    } else if (warp == 1) {
-      if (leader && lane == 0 && n_my > 0) {
         const uint32_t id0 = idesc_bf16_f32(256, N0, 0, 1);
         const uint32_t id1 = idesc_bf16_f32(256, N1 ? N1 : 128, 0, 1);
         int stage = 0;
         uint32_t ph = 0;
-        bool ok = true, first = true;
+        bool first = true;
         for (int u = 0; u < n_iter && ok; ++u) {
           const int t = consumer_tile(u, ra, rb, p.ksplit);
           if (t >= p.n_vt) continue;
           for (int ks = 0; ks < kVT / 64; ++ks) {
-            if (!wait_bar(smem_addr(&bar_full[stage]), ph, p)) { ok = false; break; }
+            if (!wait_bar(smem_addr(&bar_full2[stage]), ph, p)) { ok = false; break; }
             tc_fence_after();
-            const uint32_t sb = s_base + stage * stage_bytes;
+            const uint32_t sb = s_base + stage * stage_c;
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
               const uint32_t acc = (first && ks == 0 && k == 0) ? 0u : 1u;
@@ -930,49 +857,151 @@ __global__ void __launch_bounds__(kThreads, 1)
               mma_bf16_pair(tmem, adesc, sdesc_sw128(sb + 16384 + k * 2048, 8192, 1024), id0, acc);
               if (n_mma == 2) mma_bf16_pair(tmem + 256, adesc, sdesc_sw128(sb + e1_off + k * 2048, 8192, 1024), id1, acc);
             }
-            mma_commit_pair_mc(smem_addr(&bar_empty[stage]), 3);
-            if (++stage == n_stages) { stage = 0; ph ^= 1; }
+            mma_commit_pair_mc(smem_addr(&bar_empty2[stage]), 3);
+            if (++stage == n_stages_c) { stage = 0; ph ^= 1; }
           }
           first = false;
         }
-        mma_commit_pair_mc(smem_addr(&bar_tfull[0]), 3);
+        mma_commit_pair_mc(smem_addr(&bar_tfull[1]), 3);
+      }
+      if (n_prod > 0 || n_cons > 0) {
         mma_commit_pair_mc(smem_addr(&bar_drain), 1);
         drain_bar(smem_addr(&bar_drain), 0, p);
       }
+    }
+    __syncwarp();
+  } else {
+    // ===================================================== epilogue warps 2..9
+    // Produce phase: id half hc of the tile, TMEM lane quarter q; one row per thread.
+    const int hc = (warp - 2) >> 2;
+    const int q = warp & 3;
+    const int r = q * 32 + lane;  // row within this CTA's half = TMEM lane
+    const int i = (int)rank * 128 + r;
+    const int slot = pair * 2 + hc;
+    const uint32_t tl = tmem + ((uint32_t)(q * 32) << 16) + hc * 128;
+    float R2 = 0.f, lim2 = 0.f;
+    float m_run = -INFINITY, z_run = 0.f;
+    int a_run = 0x7fffffff;
+    bool ovf = false;
+    bool ok = true;
+    if (n_prod == 0) {
+      p.smax[(size_t)i * p.n_a + slot] = -INFINITY;
+      __threadfence();
+      epi_sync();
+      if (threadIdx.x == 64) red_release_add_gpu(p.ref_count, 1);
+    }
+    for (int j = 0; j < n_prod && ok; ++j) {
+      const int t = prod_tile(p, pair, j);
+      const int b = j & 1;
+      const bool got = wait_bar(smem_addr(&bar_tfull[b]), (uint32_t)(j >> 1) & 1u, p);
+      if (epi_any(!got)) { ok = false; break; }
+      tc_fence_after();
+      float v[128];
+      tmem_ld128(tl + b * 256, v);
+      // every logit of this half-tile is in registers: hand the buffer back
+      tc_fence_before();
       __syncwarp();
-    } else {
-      // epilogue: warp w reads accumulator m = (w-2)/4 (columns d0 + 256m ...) for its lane quarter
-      const int q = warp & 3;
-      const int m = (warp - 2) >> 2;
-      const int r = q * 32 + lane;
-      const int i = (int)rank * 128 + r;
-      if (m < n_mma) {
-        bool have = n_my > 0;
-        if (n_my > 0) {
-          bool got = wait_bar(smem_addr(&bar_tfull[0]), 0, p);
-          got = __all_sync(0xffffffffu, got);  // tcgen05.ld below is warp-collective
-          have = got;
-          tc_fence_after();
+      if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_addr(&bar_tempty[b]), 0));
+      const int vb = t * kVT + hc * 128;
+      if (vb + 128 > p.V) {
+#pragma unroll
+        for (int e = 0; e < 128; ++e)
+          if (vb + e >= p.V) v[e] = -INFINITY;
+      }
+      float bm[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) bm[e] = fmaxf(v[e], v[120 + e]);
+#pragma unroll
+      for (int bb = 8; bb < 120; bb += 16)
+#pragma unroll
+        for (int e = 0; e < 8; ++e) bm[e] = max3(bm[e], v[bb + e], v[bb + 8 + e]);
+      const float cm = max3(max3(bm[0], bm[1], bm[2]), max3(bm[3], bm[4], bm[5]), fmaxf(bm[6], bm[7]));
+      if (j == 0) {
+        // this slot's first half-tile is its sample -> grid-wide reference: one
+        // atomic max per row, read back once every CTA has contributed
+        p.smax[(size_t)i * p.n_a + slot] = cm;
+        red_max_u32(p.rowkey + i, order_key(cm));
+        __threadfence();
+        epi_sync();
+        if (threadIdx.x == 64) red_release_add_gpu(p.ref_count, 1);
+        const bool refd = wait_flag(p.ref_count, 2 * NP, p);
+        if (epi_any(!refd)) { ok = false; break; }
+        const float R = from_order_key(__ldcg(p.rowkey + i));
+        R2 = R * kLog2e;
+        lim2 = (R + kTau) * kLog2e;
+      }
+      if (cm > m_run) {
+        int ci = 127;
+#pragma unroll
+        for (int e = 127; e >= 0; --e)
+          if (v[e] == cm) ci = e;
+        m_run = cm;
+        a_run = vb + ci;
+      }
+      if (cm * kLog2e > lim2) ovf = true;
+      float zs[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) zs[e] = 0.f;
+      // P blocks [t][sub-tile of 64 ids][row half = rank], pre-swizzled K-major
+      uint8_t* prow = p.pbuf + ((size_t)((t * 4 + hc * 2) * 2 + (int)rank)) * kTileBytes + (size_t)r * 128;
+#pragma unroll
+      for (int e8 = 0; e8 < 16; ++e8) {
+        float pe[8];
+#pragma unroll
+        for (int f = 0; f < 8; f += 2) {
+          float x0, x1;
+          fma2(x0, x1, v[e8 * 8 + f], v[e8 * 8 + f + 1], kLog2e, kLog2e, -R2, -R2);
+          pe[f] = ex2_approx(x0);  // masked ids: exp2(-inf) = 0
+          pe[f + 1] = ex2_approx(x1);
+          add2(zs[f], zs[f + 1], pe[f], pe[f + 1]);
         }
-        const int Nm = m ? N1 : N0;
-        const int cend = d0 + nd;
-        float* dst = p.cpart + ((size_t)ra * 256 + i) * p.d;
-        float* dz = rb >= 0 ? p.cpart + ((size_t)rb * 256 + i) * p.d : nullptr;
-        for (int cc = 0; cc < Nm / 32; ++cc) {
-          const int col = d0 + m * 256 + cc * 32;
-          float v[32];
-          if (have) {
-            tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + m * 256 + cc * 32, v);
-          } else {
+        const int sub = e8 >> 3, piece = e8 & 7;
+        uint8_t* dst = prow + (size_t)sub * 2 * kTileBytes + ((piece ^ (r & 7)) << 4);
+        *reinterpret_cast<uint4*>(dst) =
+            make_uint4(pack2(pe[0], pe[1]), pack2(pe[2], pe[3]), pack2(pe[4], pe[5]), pack2(pe[6], pe[7]));
+      }
+      z_run += ((zs[0] + zs[1]) + (zs[2] + zs[3])) + ((zs[4] + zs[5]) + (zs[6] + zs[7]));
+      // publish this CTA's half of the P tile (consumers wait for both halves)
+      fence_proxy_async_global();
+      __threadfence();
+      epi_sync();
+      if (threadIdx.x == 64 && !(p.inject && t == 0)) red_release_add_gpu(p.ready + t, 1);
+    }
+    if (i < p.C) {
+      p.am[(size_t)i * p.n_a + slot] = m_run;
+      p.aa[(size_t)i * p.n_a + slot] = a_run;
+      p.az[(size_t)i * p.n_a + slot] = z_run;
+      if (ovf) p.overflow[i] = 1;
+    }
+    // Consume phase: warp w reads accumulator m = hc (columns d0 + 256m ...) for its lane quarter.
+    const int m = hc;
+    if (!is_a && m < n_mma) {
+      bool have = n_cons > 0 && ok;
+      if (n_cons > 0) {
+        bool got = wait_bar(smem_addr(&bar_tfull[1]), 0, p);
+        got = __all_sync(0xffffffffu, got);  // tcgen05.ld below is warp-collective
+        have = have && got;
+        tc_fence_after();
+      }
+      have = __all_sync(0xffffffffu, have);
+      const int Nm = m ? N1 : N0;
+      const int cend = d0 + nd;
+      float* dst = p.cpart + ((size_t)ra * 256 + i) * p.d;
+      float* dz = rb >= 0 ? p.cpart + ((size_t)rb * 256 + i) * p.d : nullptr;
+      for (int cc = 0; cc < Nm / 32; ++cc) {
+        const int col = d0 + m * 256 + cc * 32;
+        float v[32];
+        if (have) {
+          tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + m * 256 + cc * 32, v);
+        } else {
 #pragma unroll
-            for (int e = 0; e < 32; ++e) v[e] = 0.f;
-          }
-          if (i < p.C && col < cend) {
+          for (int e = 0; e < 32; ++e) v[e] = 0.f;
+        }
+        if (i < p.C && col < cend) {
 #pragma unroll
-            for (int e = 0; e < 32; e += 4) {
-              *reinterpret_cast<float4*>(dst + col + e) = make_float4(v[e], v[e + 1], v[e + 2], v[e + 3]);
-              if (dz) *reinterpret_cast<float4*>(dz + col + e) = make_float4(0.f, 0.f, 0.f, 0.f);
-            }
+          for (int e = 0; e < 32; e += 4) {
+            *reinterpret_cast<float4*>(dst + col + e) = make_float4(v[e], v[e + 1], v[e + 2], v[e + 3]);
+            if (dz) *reinterpret_cast<float4*>(dz + col + e) = make_float4(0.f, 0.f, 0.f, 0.f);
           }
         }
       }
@@ -1252,7 +1281,7 @@ Plan as_plan(const PairPlan& q) {
   p.n_rh = 2;
   p.n_vt = q.n_vt;
   p.ksplit = q.ksplit;
-  p.n_a = 2 * q.n_pa;  // statistics slots: (pair, id half)
+  p.n_a = 2 * (q.n_pa + q.n_pc);  // statistics slots: (pair, id half); every pair produces a tile
   p.n_c = 2 * q.n_pc;
   p.n_dt = 0;
   p.window = 1 << 30;
@@ -1316,6 +1345,7 @@ int vocab_tc_launch(const __nv_bfloat16* h, const __nv_bfloat16* emb, int C, int
   p.n_rh = pl.n_rh; p.n_dt = pl.n_dt; p.n_vt = pl.n_vt; p.ksplit = pl.ksplit; p.n_a = pl.n_a;
   p.window = pl.window;
   p.n_pa = pairs ? pq.n_pa : 0;
+  p.n_pc = pairs ? pq.n_pc : 0;
   p.n_full = pairs ? pq.n_full : 0;
   p.rem = pairs ? pq.rem : 0;
   p.n_fullx = pairs ? pq.n_fullx : 0;
@@ -1338,6 +1368,7 @@ int vocab_tc_launch(const __nv_bfloat16* h, const __nv_bfloat16* emb, int C, int
   p.ref_count = flags + 2 * pl.n_vt;
   p.abort_flag = flags + 2 * pl.n_vt + 1;
   p.overflow = flags + 2 * pl.n_vt + 2;
+  p.rowkey = (unsigned*)(flags + 2 * pl.n_vt + 2 + 256);
   p.smax = (float*)(w + L.smax);
   p.am = (float*)(w + L.am);
   p.aa = (int*)(w + L.aa);
