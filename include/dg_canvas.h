@@ -154,8 +154,10 @@ DG_API int dg_vocab_step_renoise(const void* h, const void* emb, int C, int V, i
 
 /* Launch plan of the bf16 vocabulary step on the current device (host-only
  * query, no kernel): plan[0] producer CTAs, [1] consumer CTAs, [2] vocabulary
- * split of the consumers, [3] 1 if producers run as cluster pairs sharing E by
- * multicast, [4] CTAs launched, [5] vocabulary tiles of 256 ids. */
+ * residue classes of the consumers, [3] 1 if the kernel runs on CTA pairs
+ * (clusters of two CTAs sharing each MMA; 0: one CTA per role unit, where such
+ * clusters cannot be placed), [4] CTAs launched, [5] vocabulary tiles of 256
+ * ids. The query needs no device: without one it plans for 152 SMs. */
 DG_API int dg_vocab_step_plan(int C, int V, int d, int dtype, int32_t* plan /* [6] */);
 
 /* ---------------------------------------------------------------- re-noise
