@@ -204,6 +204,8 @@ def test_vocab_form_follows_environment(lib):
     (1, 4096, 64, 0.0, 1.0),
     (256, 20000, 640, 3.0, 0.1),      # a 128-column remainder next to a full 512-column slice
     (130, 7000, 768, 2.0, 0.1),       # a 256-column remainder; two rows in the second row half
+    (256, 2000, 8192, 3.0, 0.05),     # the largest d: 32 consumer slices, one residue class
+    (256, 100, 4160, 2.0, 0.1),       # fewer ids than one tile; a 64-column remainder slice
 ])
 def test_vocab_step_bf16(lib, C, V, d, alpha, std):
     h, emb = _vocab_case(C, V, d, seed=C + V, alpha=alpha, std=std)
