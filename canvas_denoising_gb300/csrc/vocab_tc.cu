@@ -17,7 +17,7 @@
 //    fp32 range) is flagged and recomputed exactly by the combine kernel
 //    with R = its true maximum.
 //  * Two roles, all co-resident (cooperative launch, one CTA per SM):
-//    - producers own vocabulary tiles of 256 ids (round robin). GEMM1:
+//    - producers make vocabulary tiles of 256 ids (round robin). GEMM1:
 //      logits[rows x 256] = H . E_tile^T, K-loop over d in steps of 64
 //      through a TMA ring. Eight epilogue warps read the logits from TMEM,
 //      keep per-row running max / first argmax / sum of exp(l - R), and
@@ -611,10 +611,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 //    two buffers fit: the epilogue of tile j overlaps the MMAs of tile j+1.
 //    Epilogue warp w reads one 128-id half (hc) of its row in one load and
 //    keeps statistics per (pair, hc) slot.
-//  * Consumer pair: a d-slice of up to 512 columns (two MMAs of N <= 256,
-//    each CTA holding half of each N) and one residue class of tiles; the
-//    pairs of a narrow remainder slice take two residue classes each, so that
-//    every consumer pair carries about the same work.
+//  * Consumer pair: a d-slice of 256 columns (512 behind a switch: two MMAs
+//    of N = 256, each CTA holding half of each N) and one residue class of
+//    tiles; the pairs of a narrow remainder slice take two residue classes
+//    each, so that every consumer pair carries about the same work.
+//  * First round: every pair, consumer pairs included, produces the tile
+//    with its own index before anything is published, so consumers are not
+//    idle at the start; a consumer pair then switches to GEMM2, reusing the
+//    ring with barriers of its own once its GEMM1 MMAs have completed.
 // Loads of both CTAs complete on the even CTA's "full" barrier (it alone
 // issues MMAs); commits arrive on both CTAs' barriers.
 constexpr int kRingBytes = 196608;   // operand ring per CTA (6 producer stages; 7 measured no faster)
