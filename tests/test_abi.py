@@ -115,6 +115,29 @@ def test_vocab_plan_is_a_host_query(lib):
     assert lib.dg_vocab_step_plan(256, 262144, 2800, B.DG_BF16, ctypes.cast(buf, ctypes.c_void_p)) == B.DG_ERR_INVALID_ARG
 
 
+@pytest.mark.parametrize("C,V,d", [
+    (256, 262144, 2816), (256, 32768, 1024), (256, 65536, 2816), (1, 1, 64), (77, 33333, 192), (200, 9000, 320),
+    (256, 100, 4160), (256, 2000, 8192), (256, 262144, 8192), (130, 7000, 768), (256, 20000, 640), (256, 257, 64),
+])
+def test_vocab_plans_are_consistent(lib, C, V, d):
+    """For shapes across the supported range: both roles present, the grid
+    fits the GPU (152 SMs without a device), CTA pairs come in twos, the
+    residue classes do not outnumber the tiles, and the workspace holds at
+    least the P ring and the consumers' fp32 partials."""
+    plan = B.vocab_step_plan(C, V, d)
+    n_vt = (V + 255) // 256
+    assert plan["vocab_tiles"] == n_vt
+    assert plan["producers"] >= 1 and plan["consumers"] >= 1
+    assert plan["producers"] + plan["consumers"] == plan["ctas"] <= 152
+    assert 1 <= plan["vocab_split"] <= n_vt
+    if plan["cluster_pairs"]:
+        assert plan["producers"] % 2 == 0 and plan["consumers"] % 2 == 0
+        assert plan["producers"] // 2 <= n_vt
+    ring = n_vt * 256 * 256 * 2                 # bf16 P for every row and vocabulary id
+    partials = plan["vocab_split"] * 256 * d * 4
+    assert B.vocab_step_workspace_size(C, V, d) >= ring + partials
+
+
 def test_debug_inject_validates(lib):
     assert lib.dg_debug_inject(7, 0) == B.DG_ERR_INVALID_ARG
     assert lib.dg_debug_inject(1, -1) == B.DG_ERR_INVALID_ARG
