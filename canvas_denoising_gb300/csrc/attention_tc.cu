@@ -780,6 +780,8 @@ int attn_tc_launch(const void* q, const void* k_cache, const void* v_cache, int6
   at[0].val.cooperative = 1;
   cfg.attrs = at;
   cfg.numAttrs = splits > 1 ? 1 : 0;
+  // The arrival counters start at zero on every call; dg_canvas_attn_noalloc
+  // relies on this memset, since its shared scratch keeps the previous call's counts.
   if (splits > 1) DG_CUDA_TRY(cudaMemsetAsync(a.arrived, 0, (size_t)L.groups * sizeof(int), s));
   DG_CUDA_TRY(cudaLaunchKernelEx(&cfg, attn_fwd_tc, tk_c, tv_c, tk_n, tv_n, tq, a));
   return DG_OK;

@@ -1,24 +1,25 @@
 // dg_canvas_attn_noalloc: canvas attention without a caller-provided workspace.
 //
 // Some callers cannot allocate device memory at the moment they run attention:
-// code that executes while a stream is being captured into a CUDA graph (an
-// allocation there would break or invalidate the capture), hosts whose memory
-// manager owns every device allocation and forbids side allocations, and
-// plugins that are handed tensors but no scratch buffer. For them this entry
-// point keeps its split-KV scratch in a fixed array in device memory that is
-// part of the library image itself.
+// hosts whose memory manager owns every device allocation and forbids side
+// allocations, plugins that are handed tensors but no scratch buffer, and
+// latency-critical loops where a cudaMalloc could synchronise the device. For
+// them this entry point keeps its split-KV scratch in a fixed array in device
+// memory that is part of the library image itself.
 //
 // The array is kAttnScratchBytes (32 MiB). Every GPU that loads the library
 // keeps that memory reserved until the process exits. All calls share the one
 // array: calls that can overlap on the GPU (different streams without
-// ordering between them) race on it and must not be issued. Nothing in the
-// array has to start at zero: each call writes every partial result before it
-// reads it, so the contents left by the previous call do not matter.
+// ordering between them) race on it and must not be issued. The contents left
+// by the previous call do not matter: the call zeroes the per-group arrival
+// counters it needs with a stream-ordered memset before its launch (the same
+// memset the workspace entry point issues), and every partial result is
+// written before it is read.
 //
 // Host code cannot use the array's name as a device address (in host code it
 // names a host-side shadow). The device address is looked up with
 // cudaGetSymbolAddress once per device, on the first call made while that
-// device is current; that first call must therefore come before any stream
+// device is current; that first call should therefore come before any stream
 // capture begins on the device.
 #include <mutex>
 

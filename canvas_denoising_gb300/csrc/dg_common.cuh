@@ -16,7 +16,7 @@ __device__ __forceinline__ void latch(int* status, int code) {
   if (status) atomicCAS(status, 0, code);
 }
 
-int* status_ptr();
+int* status_ptr();  // device address of the status word for the current device (api.cu)
 
 // Host-side failure injection for tests (dg_debug_inject): the next launch of
 // the named kernel withholds one arrival, so its peers' bounded waits expire.
@@ -25,7 +25,7 @@ struct Inject {
   int kind;
   long long wait_cycles;  // bound for that launch's waits (0: the default)
 };
-Inject take_inject(int kind);  // returns and clears the pending injection if it is `kind`  // device address of the status word for the current device (api.cu)
+Inject take_inject(int kind);  // returns and clears the pending injection if it is `kind`
 
 // Reports a failed CUDA call on stderr when DG_VERBOSE is set (defined in api.cu).
 void report_cuda_error(cudaError_t e, const char* what, const char* file, int line);

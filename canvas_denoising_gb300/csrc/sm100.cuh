@@ -238,25 +238,6 @@ __device__ __forceinline__ uint32_t cluster_ctarank() {
 __device__ __forceinline__ void cluster_sync() {
   asm volatile("barrier.cluster.arrive.release.aligned;\nbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
-// TMA tile load delivered to the same shared-memory offset in every CTA of
-// `mask`, completing bytes on the mbarrier at `bar` in each of them.
-__device__ __forceinline__ void tma_load_2d_mc(uint32_t dst, const CUtensorMap* map, int32_t x, int32_t y,
-                                               uint32_t bar, uint16_t mask, uint64_t policy) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster.L2::"
-      "cache_hint [%0], [%1, {%2, %3}], [%4], %5, %6;" ::"r"(dst),
-      "l"(map), "r"(x), "r"(y), "r"(bar), "h"(mask), "l"(policy)
-      : "memory");
-}
-// Arrives on the mbarrier at `bar` in every CTA of `mask` once this thread's
-// issued tcgen05.mma operations have completed.
-__device__ __forceinline__ void mma_commit_mc(uint32_t bar, uint16_t mask) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
-                   bar),
-               "h"(mask)
-               : "memory");
-}
-
 }  // namespace sm100
 }  // namespace dg
 

@@ -1,6 +1,8 @@
 """The allocation-free attention entry point (for callers that cannot call
-cudaMalloc, e.g. while a stream is being captured, or inside a host that owns
-all device memory) must give the same results as the workspace entry point.
+cudaMalloc: a host whose memory manager owns all device memory, a plugin
+handed no scratch buffer) must give the same results as the workspace entry
+point, call after call, although its scratch array keeps the last call's
+contents.
 
 This file sorts last so that a run stopping at its first failure has already
 run every other test; it must also pass alone in a fresh process.
