@@ -554,10 +554,7 @@ def run_ours(args, world, rank, local):
         "warmup": args.warmup, "ms_per_step": round(ms / K, 5), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16" if w.dtype == "bf16" else "f32", "data": "synthetic",
         "canvas_tok_per_s": round(steps_per_s * w.C, 1),
-        "config": {"workload": w.name, "canvas": w.C, "vocab": w.V, "d_model": w.d, "q_heads": w.Hq,
-                   "kv_heads": w.Hkv, "head_dim": w.hd, "kv_prefix": w.prefix, "threshold": w.thresholds[0],
-                   "steps_per_canvas": w.steps, "alpha": w.alpha, "parallelism": f"replicas{world}",
-                   "l2": l2_label(w)},
+        "config": workload_config(w, world),
         "roofline": roof,
         "roofline_attention": roof_attn,
         "gpu_launches": launches * world,
@@ -581,6 +578,13 @@ def run_ours(args, world, rank, local):
     if world > 1:
         torch.distributed.destroy_process_group()
     return line
+
+
+def workload_config(w, world):
+    """The `config` object of the JSON line (the same for both arms)."""
+    return {"workload": w.name, "canvas": w.C, "vocab": w.V, "d_model": w.d, "q_heads": w.Hq, "kv_heads": w.Hkv,
+            "head_dim": w.hd, "kv_prefix": w.prefix, "threshold": w.thresholds[0], "steps_per_canvas": w.steps,
+            "alpha": w.alpha, "parallelism": f"replicas{world}", "l2": l2_label(w)}
 
 
 def capture_canvas_graph(cv, stream, spc):
@@ -696,7 +700,7 @@ def run_reference(args, world, rank, local):
     ratio, not by its share of the work: one whole step and one sample step
     are timed first; each of the W + K steps then runs the sample, sized so
     that the run takes about REF_BUDGET_S seconds, and its time is scaled by
-    that ratio."""
+    that ratio. Both calibration times are the faster of two runs."""
     if rank != 0:
         return None
     w = WORKLOADS[args.workload]
@@ -711,9 +715,10 @@ def run_reference(args, world, rank, local):
         h = synth.hidden(emb, tgt, w.alpha, w.seed, step=s, dtype=dt)
         q, kn, vn = synth.canvas_qkv(w.C, w.Hq, w.Hkv, w.hd, w.seed, step=s, dtype=dt)
         ins.append(tuple(x.float().numpy() for x in (h, q, kn, vn)))
-    t_full = oracle_step_parts(w, emb_np, k_np, v_np, ins[0], w.C, w.V, w.seed, 0)
+    # the faster of two whole steps (the first call also pays for cold pages)
+    t_full = min(oracle_step_parts(w, emb_np, k_np, v_np, ins[i], w.C, w.V, w.seed, i) for i in range(2))
     n = args.steps + args.warmup
-    per_step = min(t_full, (REF_BUDGET_S - t_full) / max(1, n))
+    per_step = min(t_full, (REF_BUDGET_S - 2 * t_full) / max(1, n))
     if per_step >= t_full:
         qa, Vs = w.C, w.V  # the whole step fits the budget
     else:
@@ -721,7 +726,7 @@ def run_reference(args, world, rank, local):
         frac = max(per_step, 1e-3) / t_full
         Vs = max(min(w.V, 256), min(w.V, int(w.V * frac) // 256 * 256))
         qa = max(1, min(w.C, int(w.C * frac)))
-    t_cal = oracle_step_parts(w, emb_np, k_np, v_np, ins[1], qa, Vs, w.seed, 1)
+    t_cal = min(oracle_step_parts(w, emb_np, k_np, v_np, ins[i], qa, Vs, w.seed, i) for i in range(2))
     scale = t_full / t_cal
     for s in range(args.warmup):
         oracle_step_parts(w, emb_np, k_np, v_np, ins[s % 2], qa, Vs, w.seed, s)
@@ -732,11 +737,11 @@ def run_reference(args, world, rank, local):
     sample = ("whole steps" if (qa, Vs) == (w.C, w.V) else
               f"per step: attention for {qa} of {w.C} canvas positions (every head), the vocabulary step on all "
               f"{w.C} rows over {Vs} of {w.V} ids, the re-noise in full (float64 numpy), scaled x{scale:.3g} = one "
-              f"whole step ({t_full:.2f} s) / the same sample ({t_cal:.3f} s), both timed first")
+              f"whole step ({t_full:.2f} s) / the same sample ({t_cal:.3f} s), each the faster of two, timed first")
     return {"impl": "reference", "metric": metric_name(), "value": round(val, 6), "unit": "steps/s",
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * total / args.steps, 3),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": w.name, "canvas": w.C, "vocab": w.V, "d_model": w.d, "kv_prefix": w.prefix},
+            "config": workload_config(w, world),
             "cpu_baseline": {"value": round(val, 6), "unit": "steps/s", "cores": os.cpu_count(), "kind": "oracle",
                              "sample": sample},
             "e2e": {"value": round(val, 6), "unit": "steps/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}

@@ -150,7 +150,8 @@ class GraphedBlockDiffusion:
     diffusion)"). The backbone's per-step tensors are read from fixed buffers,
     which the caller fills before each replay (`load_block`)."""
 
-    def __init__(self, emb, k_cache, v_cache, prefix_len, C, Hq, threshold, seed, steps, stream, events=None):
+    def __init__(self, emb, k_cache, v_cache, prefix_len, C, Hq, threshold, seed, steps, stream, events=None,
+                 record=False):
         self.emb, self.k_cache, self.v_cache = emb, k_cache, v_cache
         self.Hkv, self.cap, self.hd = k_cache.shape
         self.V, self.d = emb.shape
@@ -181,6 +182,18 @@ class GraphedBlockDiffusion:
         self.graph = None
         self.events = events  # optional per-step (attn start, attn end, vocab start, vocab end) timing events
         self.launches = 1 + 3 * steps + 2  # kernels per canvas: init, steps x (attention + vocab 2), append 2
+        # record=True: every step's tokens, flags and statistics are copied (device to device, inside
+        # the graph) into per-step history buffers, so a whole canvas can be inspected step by step
+        self.history = None
+        if record:
+            self.history = {
+                "tokens": torch.empty((steps, C), dtype=torch.int32, device=dev),
+                "renoised": torch.empty((steps, C), dtype=torch.uint8, device=dev),
+                "argmax": torch.empty((steps, C), dtype=torch.int32, device=dev),
+                "conf": torch.empty((steps, C), dtype=torch.float32, device=dev),
+                "lse": torch.empty((steps, C), dtype=torch.float32, device=dev),
+                "attn_lse": torch.empty((steps, Hq, C), dtype=torch.float32, device=dev),
+            }
 
     def _canvas(self):
         o, s_, ev = self.out, self.stream, self.events
@@ -197,6 +210,15 @@ class GraphedBlockDiffusion:
                                         o.argmax, o.conf, o.lse, o.selfcond, o.renoised, self.ws_vocab, stream=s_)
             if ev is not None:
                 ev[s][3].record(s_)
+            if self.history is not None:
+                hist = self.history
+                with torch.cuda.stream(s_):
+                    hist["tokens"][s].copy_(self.tokens)
+                    hist["renoised"][s].copy_(o.renoised)
+                    hist["argmax"][s].copy_(o.argmax)
+                    hist["conf"][s].copy_(o.conf)
+                    hist["lse"][s].copy_(o.lse)
+                    hist["attn_lse"][s].copy_(o.attn_lse)
         B.kv_append_devlen(self.k_cache, self.v_cache, self.len_dev, self.kc[self.steps], self.vc[self.steps],
                            stream=s_)
 

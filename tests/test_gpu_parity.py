@@ -183,6 +183,10 @@ def _check_vocab(h, emb, res, ref):
     flags = logit_gap_flags(ref)
     ok = (am == ref["argmax"]) | flags
     assert ok.all(), f"argmax mismatch at rows {np.nonzero(~ok)[0][:8]}"
+    # a flagged row may differ, but rarely: a kernel that gets near-ties wrong systematically
+    # must not hide behind the flag
+    n_diff = int((am != ref["argmax"]).sum())
+    assert n_diff <= max(1, int(FLAG_BUDGET * flags.size)), f"argmax differs at {n_diff} flagged rows"
     np.testing.assert_allclose(conf, ref["conf"], rtol=CONF_REL)
     assert np.abs(lse - ref["lse"]).max() <= LSE_ABS
     assert_rows_close(sc, ref["selfcond"], what="selfcond")
@@ -287,9 +291,12 @@ def test_vocab_step_full_size_sampled_rows(lib, name):
     _check_vocab(None, None, [torch.from_numpy(g) for g in got], ref)
 
 
-# ------------------------------------------------------------------ one whole step, teacher-forced
+# ------------------------------------------------------------------ whole steps, every row
 @pytest.mark.parametrize("name", ["tiny_f32", "v32k_d1024_p1k"])
 def test_denoise_steps_match_oracle(lib, name):
+    """Every step of the workload (4 and 8): attention, the fused vocabulary
+    step + re-noise (the call the benchmark times) on every row, against the
+    oracle; flagged decisions within the 0.5% budget."""
     w = WORKLOADS[name]
     dt = torch.float32 if w.dtype == "f32" else torch.bfloat16
     emb = synth.embedding(w.V, w.d, w.seed, dtype=dt)
@@ -298,24 +305,32 @@ def test_denoise_steps_match_oracle(lib, name):
     emb_d, k_d, v_d = emb.cuda(), k.cuda(), v.cuda()
     thr = w.thresholds[0]
     tokens = torch.empty(w.C, dtype=torch.int32, device="cuda")
+    rn = torch.empty(w.C, dtype=torch.uint8, device="cuda")
     B.canvas_init(tokens, w.V, w.seed, w.prefix)
     np.testing.assert_array_equal(_np(tokens), oracle.canvas_init(w.C, w.V, w.seed, w.prefix))
+    tol = 1e-4 if dt == torch.float32 else 2e-2
+    lse_tol = 1e-4 if dt == torch.float32 else LSE_ABS
     flagged = total = 0
-    for step in range(min(w.steps, 3)):
+    for step in range(w.steps):
         q, kn, vn = synth.canvas_qkv(w.C, w.Hq, w.Hkv, w.hd, w.seed, step=step, dtype=dt)
         h = synth.hidden(emb, tgt, w.alpha, w.seed, step=step, dtype=dt)
         out, lse = B.canvas_attn(q.cuda(), k_d, v_d, w.prefix, kn.cuda(), vn.cuda())
-        am, conf, vl, sc = B.vocab_step(h.cuda(), emb_d)
-        B.renoise(tokens, am, conf, w.V, thr, w.seed, step, w.prefix)
+        am, conf, vl, sc = B.vocab_step_renoise(h.cuda(), emb_d, tokens, thr, w.seed, step, w.prefix, renoised=rn)
         ro, rl = oracle.canvas_attention(_np(q), _np(k), _np(v), w.prefix, _np(kn), _np(vn))
-        tol = 1e-4 if dt == torch.float32 else 2e-2
         assert_rows_close(_np(out).reshape(-1, w.hd), ro.reshape(-1, w.hd), tol=tol)
+        assert np.abs(_np(lse) - rl).max() <= lse_tol
         rv = oracle.vocab_step(_np(h), _np(emb))
-        ref_tok, _ = oracle.renoise(rv["argmax"], rv["conf"].astype(np.float32), w.V, thr, w.seed, step, w.prefix)
+        ref_tok, ref_rn = oracle.renoise(rv["argmax"], rv["conf"].astype(np.float32), w.V, thr, w.seed, step,
+                                         w.prefix)
         fl = decision_flags(rv, thr)
-        got = _np(tokens)
-        assert ((got == ref_tok) | fl).all()
-        flagged += int(fl.sum())
+        gap = logit_gap_flags(rv)
+        assert ((_np(tokens) == ref_tok) | fl).all()
+        assert ((_np(rn) == ref_rn) | fl).all()
+        assert ((_np(am) == rv["argmax"]) | fl | gap).all()
+        np.testing.assert_allclose(_np(conf), rv["conf"], rtol=1e-4 if dt == torch.float32 else CONF_REL)
+        assert np.abs(_np(vl) - rv["lse"]).max() <= lse_tol
+        flagged += int((fl | gap).sum())
         total += w.C
         assert_rows_close(_np(sc), rv["selfcond"], tol=tol)
     assert flagged <= FLAG_BUDGET * total, f"{flagged}/{total} flagged"
+    _status_ok()
