@@ -678,13 +678,7 @@ int key_tiles(int C, int64_t P) { return (int)((P + kBN - 1) / kBN) + (C + kBN -
 int max_splits(int C, int Hq, int Hkv, int64_t P) {
   const int64_t M = (int64_t)(Hq / Hkv) * C;
   const int64_t base = ((M + kBM - 1) / kBM) * Hkv;
-  static const int env_splits = [] {
-    const char* v = getenv("DG_ATTN_SPLITS");  // tuning knob: force the number of key splits
-    const int x = v ? atoi(v) : 0;
-    return x > 0 ? x : 0;
-  }();
   int want = (int)(num_sms() / base);
-  if (env_splits && env_splits < want) want = env_splits;
   const int tiles = key_tiles(C, P);
   if (want > tiles) want = tiles;
   if (want > kMaxSplits) want = kMaxSplits;

@@ -71,7 +71,7 @@ constexpr float kTau = 40.f;       // overflow margin above the reference, natur
 constexpr long long kTimeoutCycles = 4000000000ll;
 
 struct Plan {
-  int n_rh, n_dt, n_vt, ksplit, n_a, n_c, window;
+  int n_rh, n_dt, n_vt, ksplit, n_a, n_c;
 };
 
 // Optional integer override from the environment (tuning knobs, read once).
@@ -103,8 +103,7 @@ Plan make_plan(int C, int V, int d) {
   p.n_vt = (V + kVT - 1) / kVT;
   const int sms = num_sms();
   const int tiles_c = p.n_dt;  // a consumer CTA covers every row for its d-slice
-  static const int ks_env = env_int("DG_VOCAB_KSPLIT", 0);
-  int ks = ks_env ? ks_env : (int)lround((double)(sms / 2) / tiles_c);
+  int ks = (int)lround((double)(sms / 2) / tiles_c);
   if (ks < 1) ks = 1;
   if (ks > p.n_vt) ks = p.n_vt;
   while (ks > 1 && tiles_c * ks > sms - 1) --ks;
@@ -113,17 +112,6 @@ Plan make_plan(int C, int V, int d) {
   p.n_a = sms - p.n_c;
   if (p.n_a > p.n_vt) p.n_a = p.n_vt;
   if (p.n_a < 1) p.n_a = 1;
-  // Producers may run at most `window` tiles ahead of the slowest consumer, so
-  // that the E rows a consumer reads are still in L2 (about 80 MB of E in flight).
-  static const int win_env = env_int("DG_VOCAB_WINDOW", 0);
-  const double tile_bytes = (double)kVT * d * 2;
-  int win = (int)(80e6 / tile_bytes);
-  if (win > 2 * p.n_a) win = 2 * p.n_a;
-  if (win < p.n_a + 16) win = p.n_a + 16;
-  // Measured: coupling producers to the slowest consumer costs more than the
-  // re-reads it saves, so the window is off unless DG_VOCAB_WINDOW sets one.
-  (void)win;
-  p.window = win_env ? (win_env > p.n_a ? win_env : p.n_a + 1) : (1 << 30);
   return p;
 }
 
@@ -138,7 +126,7 @@ Layout make_layout(const Plan& p, int d) {
   Layout L;
   size_t o = 0;
   L.flags = o;
-  L.flag_bytes = (size_t)(2 * p.n_vt + 2 + 256 + 256) * sizeof(int);  // + per-row reference keys
+  L.flag_bytes = (size_t)(p.n_vt + 2 + 256 + 256) * sizeof(int);  // + per-row reference keys
   o += up256(L.flag_bytes);
   L.smax = o; o += up256((size_t)p.n_a * 256 * 4);
   L.am = o;   o += up256((size_t)p.n_a * 256 * 4);
@@ -151,10 +139,8 @@ Layout make_layout(const Plan& p, int d) {
 }
 
 struct Params {
-  int C, V, d, n_rh, n_dt, n_vt, ksplit, n_a, window;
-  int l2hint;      // 1: producer E loads evict_last, consumer E/P loads evict_first
+  int C, V, d, n_rh, n_dt, n_vt, ksplit, n_a;
   int* ready;      // [n_vt] tile published counters
-  int* consumed;   // [n_vt] consumer CTAs that have fetched the tile
   int* ref_count;  // producers that have published their sample maxima
   int* abort_flag;
   int* overflow;   // [256]
@@ -177,12 +163,12 @@ struct Params {
   long long wait_cycles;       // bound of every wait
   int* status;
   // paired form only: producer pairs, and the consumer pairs' d-slicing
-  // (n_full slices of 512 columns, then a remainder of `rem` columns; see consumer_slice)
+  // (n_full slices of cw = 256 columns, then a remainder of `rem` columns; see consumer_slice)
   int n_pa, n_pc, n_full, rem, n_fullx, cw;
-  // paired form: L2 policy per operand stream (H, producer E, P, consumer E):
-  // 0 none, 1 evict_last, 2 evict_first, 3 evict_normal
-  int pol[4];
   int ring_bytes;  // paired form: operand ring per CTA (a multiple of 32 KB)
+  // paired form, produce phase: consumer pair ci makes tile cb + ci in the first round; producer
+  // pair a makes tile a, then pb + a + (j-1) n_pa for j >= 1 while below pe
+  int cb, pb, pe;
 };
 
 __device__ __forceinline__ bool aborted(const int* f) { return *(volatile const int*)f != 0; }
@@ -305,24 +291,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int s = 0; s < kStages; ++s) issued[s] = false, issued_par[s] = 0;
         const uint32_t tx = (uint32_t)p.n_rh * kTileBytes + kEBytesA;
         const uint64_t pol_last = policy_evict_last();
-        const int n_cons = p.n_dt;  // consumer CTAs per tile
         bool ok = true;
         for (int j = 0; j < n_my && ok; ++j) {
           const int t = a + j * p.n_a;
-          if (t >= p.window && !wait_flag(p.consumed + (t - p.window), n_cons, p)) break;
           for (int ks = 0; ks < ksteps_d; ++ks) {
             if (!wait_bar(smem_addr(&bar_empty[stage]), ph ^ 1, p)) { ok = false; break; }
             const uint32_t fb = smem_addr(&bar_full[stage]);
             const uint32_t sb = s_base + stage * kStageBytes;
             mbar_expect_tx(fb, tx);
-            if (p.l2hint) {
-              for (int h = 0; h < p.n_rh; ++h)
-                tma_load_2d_hint(sb + h * kTileBytes, &tm_h, ks * kBK, h * 128, fb, pol_last);
-              tma_load_2d_hint(sb + 2 * kTileBytes, &tm_ek, ks * kBK, t * kVT, fb, pol_last);
-            } else {
-              for (int h = 0; h < p.n_rh; ++h) tma_load_2d(sb + h * kTileBytes, &tm_h, ks * kBK, h * 128, fb);
-              tma_load_2d(sb + 2 * kTileBytes, &tm_ek, ks * kBK, t * kVT, fb);
-            }
+            for (int h = 0; h < p.n_rh; ++h)
+              tma_load_2d_hint(sb + h * kTileBytes, &tm_h, ks * kBK, h * 128, fb, pol_last);
+            tma_load_2d_hint(sb + 2 * kTileBytes, &tm_ek, ks * kBK, t * kVT, fb, pol_last);
             issued[stage] = true;
             issued_par[stage] = ph;
             if (++stage == kStages) { stage = 0; ph ^= 1; }
@@ -513,21 +492,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t fb = smem_addr(&bar_full[stage]);
             const uint32_t sb = s_base + stage * kStageBytes;
             mbar_expect_tx(fb, tx);
-            if (p.l2hint) {
-              bulk_load_hint(sb, p.pbuf + (size_t)((t * 4 + ks) * p.n_rh) * kTileBytes, pbytes, fb, pol_first);
-              for (int bx = 0; bx < nbox; ++bx)
-                tma_load_2d_hint(sb + 2 * kTileBytes + bx * 8192, &tm_emn, d0 + bx * 64, t * kVT + ks * 64, fb,
-                                 pol_first);
-            } else {
-              bulk_load(sb, p.pbuf + (size_t)((t * 4 + ks) * p.n_rh) * kTileBytes, pbytes, fb);
-              for (int bx = 0; bx < nbox; ++bx)
-                tma_load_2d(sb + 2 * kTileBytes + bx * 8192, &tm_emn, d0 + bx * 64, t * kVT + ks * 64, fb);
-            }
+            bulk_load_hint(sb, p.pbuf + (size_t)((t * 4 + ks) * p.n_rh) * kTileBytes, pbytes, fb, pol_first);
+            for (int bx = 0; bx < nbox; ++bx)
+              tma_load_2d_hint(sb + 2 * kTileBytes + bx * 8192, &tm_emn, d0 + bx * 64, t * kVT + ks * 64, fb,
+                               pol_first);
             issued[stage] = true;
             issued_par[stage] = ph;
             if (++stage == kStages) { stage = 0; ph ^= 1; }
           }
-          if (ok) atomicAdd(p.consumed + t, 1);
         }
         for (int s = 0; s < kStages; ++s)
           if (issued[s]) drain_bar(smem_addr(&bar_full[s]), issued_par[s], p);
@@ -611,10 +583,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 //    two buffers fit: the epilogue of tile j overlaps the MMAs of tile j+1.
 //    Epilogue warp w reads one 128-id half (hc) of its row in one load and
 //    keeps statistics per (pair, hc) slot.
-//  * Consumer pair: a d-slice of 256 columns (512 behind a switch: two MMAs
-//    of N = 256, each CTA holding half of each N) and one residue class of
-//    tiles; the pairs of a narrow remainder slice take two residue classes
-//    each, so that every consumer pair carries about the same work.
+//  * Consumer pair: a d-slice of 256 columns (one MMA of N = 256, each CTA
+//    holding half of N) and one residue class of tiles; the pairs of a
+//    narrow remainder slice take two residue classes each, so that every
+//    consumer pair carries about the same work.
 //  * First round: every pair, consumer pairs included, produces the tile
 //    with its own index before anything is published, so consumers are not
 //    idle at the start; a consumer pair then switches to GEMM2, reusing the
@@ -660,35 +632,20 @@ __device__ __forceinline__ void red_max_u32(unsigned* a, unsigned v) {
   asm volatile("red.relaxed.gpu.global.max.u32 [%0], %1;" ::"l"(a), "r"(v) : "memory");
 }
 
-// j-th tile a pair produces: its own index first (every pair takes part in the
-// first round), then, for producer pairs, every n_pa-th tile after the first round.
+// j-th tile a pair produces. Every pair takes part in the first round: producer
+// pair a makes tile a, consumer pair ci tile cb + ci; producer pairs then
+// continue with every n_pa-th tile from pb + a (below pe).
 __device__ __forceinline__ int prod_tile(const Params& p, int pair, int j) {
-  return j == 0 ? pair : p.n_pa + p.n_pc + pair + (j - 1) * p.n_pa;
+  if (pair >= p.n_pa) return p.cb + (pair - p.n_pa);
+  return j == 0 ? pair : p.pb + pair + (j - 1) * p.n_pa;
 }
+
 
 // u-th tile of a consumer pair (ascending; may exceed n_vt, which callers skip).
 __device__ __forceinline__ int consumer_tile(int u, int ra, int rb, int ks) {
   return rb < 0 ? ra + u * ks : (u >> 1) * ks + ((u & 1) ? rb : ra);
 }
 
-__device__ __forceinline__ uint64_t make_policy(int kind) {
-  uint64_t r = 0;
-  if (kind == 1)
-    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(r));
-  else if (kind == 2)
-    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(r));
-  else if (kind == 3)
-    asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(r));
-  return r;
-}
-
-__device__ __forceinline__ void pair_load(uint32_t dst, const CUtensorMap* map, int x, int y, uint32_t bar,
-                                          bool hint, uint64_t pol) {
-  if (hint)
-    tma_load_2d_pair_hint(dst, map, x, y, bar, pol);
-  else
-    tma_load_2d_pair(dst, map, x, y, bar);
-}
 
 __global__ void __launch_bounds__(kThreads, 1)
     vocab_pair(const __grid_constant__ CUtensorMap tm_h, const __grid_constant__ CUtensorMap tm_ek,
@@ -737,19 +694,19 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int NP = p.n_pa + p.n_pc;
   const int ksteps_d = p.d / kBK;
   const int n_stages_a = p.ring_bytes / (int)kStageA2;
-  // Produce phase (every pair): a pair's first tile is its pair index, so the
-  // first round covers NP tiles while nothing has been published for the
-  // consumers yet; producer pairs then continue with NP + pair + (j-1)*n_pa.
-  int n_prod = pair < p.n_vt ? 1 : 0;
-  if (is_a && NP + pair < p.n_vt) n_prod += (p.n_vt - NP - pair + p.n_pa - 1) / p.n_pa;
+  // Produce phase (every pair takes part in the first round, see prod_tile).
+  int n_prod;
+  if (is_a) {
+    n_prod = pair < p.n_vt ? 1 : 0;
+    if (p.pb + pair < p.pe) n_prod += (p.pe - p.pb - pair + p.n_pa - 1) / p.n_pa;
+  } else {
+    n_prod = p.cb + (pair - p.n_pa) < p.n_vt ? 1 : 0;
+  }
   // Consume phase (consumer pairs): a d-slice and residue class(es) of tiles.
   int d0 = 0, nd = 256, ra = 0, rb = -1;
   if (!is_a) consumer_slice(p, pair - p.n_pa, d0, nd, ra, rb);
-  const int n_mma = nd > 256 ? 2 : 1;
-  const int N0 = nd >= 256 ? 256 : (nd <= 128 ? 128 : 256);
-  const int N1 = n_mma == 2 ? (nd - 256 <= 128 ? 128 : 256) : 0;
-  const uint32_t e1_off = 16384u + (uint32_t)(N0 / 128) * 8192u;  // E block of the second MMA
-  const uint32_t stage_c = e1_off + (uint32_t)(N1 / 128) * 8192u;
+  const int N0 = nd <= 128 ? 128 : 256;                          // MMA width of the slice
+  const uint32_t stage_c = 16384u + (uint32_t)(N0 / 128) * 8192u;  // P block + E block
   const int n_stages_c = p.ring_bytes / (int)stage_c < kMaxRing ? p.ring_bytes / (int)stage_c : kMaxRing;
   const int cnt_a = !is_a && ra < p.n_vt ? (p.n_vt - ra + p.ksplit - 1) / p.ksplit : 0;
   const int cnt_b = !is_a && rb >= 0 && rb < p.n_vt ? (p.n_vt - rb + p.ksplit - 1) / p.ksplit : 0;
@@ -761,7 +718,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       bool ok = true;
       if (n_prod > 0) {
-        const uint64_t pol_h = make_policy(p.pol[0]), pol_e = make_policy(p.pol[1]);
+        // L2 policies (measured: 0.540 ms with, 0.563 ms without at V = 262144): H and the producers'
+        // E rows evict_last; P and the consumers' E rows evict_first
+        const uint64_t pol_h = policy_evict_last(), pol_e = policy_evict_last();
         int stage = 0;
         uint32_t ph = 0;
         for (int j = 0; j < n_prod && ok; ++j) {
@@ -772,8 +731,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t fl = mapa_shared(fb, 0);
             const uint32_t sb = s_base + stage * kStageA2;
             if (leader) mbar_expect_tx(fb, 2 * kStageA2);
-            pair_load(sb, &tm_h, ks * kBK, (int)rank * 128, fl, p.pol[0] != 0, pol_h);
-            pair_load(sb + 16384, &tm_ek, ks * kBK, t * kVT + (int)rank * 128, fl, p.pol[1] != 0, pol_e);
+            tma_load_2d_pair_hint(sb, &tm_h, ks * kBK, (int)rank * 128, fl, pol_h);
+            tma_load_2d_pair_hint(sb + 16384, &tm_ek, ks * kBK, t * kVT + (int)rank * 128, fl, pol_e);
             if (++stage == n_stages_a) { stage = 0; ph ^= 1; }
           }
         }
@@ -781,7 +740,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (ok && n_cons > 0) {
         // the ring is reused with its own barriers: the produce phase's MMAs must have read it
         if (n_prod > 0 && !wait_bar(smem_addr(&bar_tfull[0]), 0, p)) ok = false;
-        const uint64_t pol_p = make_policy(p.pol[2]), pol_e = make_policy(p.pol[3]);
+        const uint64_t pol_p = policy_evict_first(), pol_e = policy_evict_first();
         int stage = 0;
         uint32_t ph = 0;
         for (int u = 0; u < n_iter && ok; ++u) {
@@ -795,14 +754,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t fl = mapa_shared(fb, 0);
             const uint32_t sb = s_base + stage * stage_c;
             if (leader) mbar_expect_tx(fb, 2 * stage_c);
-            pair_load(sb, &tm_p, 0, ((t * 4 + ks) * 2 + (int)rank) * 128, fl, p.pol[2] != 0, pol_p);
-            for (int m = 0; m < n_mma; ++m) {
-              const int Nm = m ? N1 : N0;
-              const uint32_t eb = sb + (m ? e1_off : 16384u);
-              for (int bx = 0; bx < Nm / 128; ++bx)
-                pair_load(eb + bx * 8192, &tm_emn, d0 + m * 256 + (int)rank * (Nm / 2) + bx * 64, t * kVT + ks * 64,
-                          fl, p.pol[3] != 0, pol_e);
-            }
+            tma_load_2d_pair_hint(sb, &tm_p, 0, ((t * 4 + ks) * 2 + (int)rank) * 128, fl, pol_p);
+            for (int bx = 0; bx < N0 / 128; ++bx)
+              tma_load_2d_pair_hint(sb + 16384 + bx * 8192, &tm_emn, d0 + (int)rank * (N0 / 2) + bx * 64,
+                                    t * kVT + ks * 64, fl, pol_e);
             if (++stage == n_stages_c) { stage = 0; ph ^= 1; }
           }
         }
@@ -838,12 +793,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       if (ok && n_cons > 0) {
-        // GEMM2: S_slice += P . E into accumulators at columns 0 (and 256), over buffer 0 of the
-        // produce phase: both CTAs' epilogues must have read that tile's logits
+        // GEMM2: S_slice += P . E into the accumulator at column 0, over buffer 0 of the produce
+        // phase: both CTAs' epilogues must have read that tile's logits
         if (n_prod > 0 && !wait_bar(smem_addr(&bar_tempty[0]), 0, p)) ok = false;
         tc_fence_after();
         const uint32_t id0 = idesc_bf16_f32(256, N0, 0, 1);
-        const uint32_t id1 = idesc_bf16_f32(256, N1 ? N1 : 128, 0, 1);
         int stage = 0;
         uint32_t ph = 0;
         bool first = true;
@@ -859,7 +813,6 @@ __global__ void __launch_bounds__(kThreads, 1)
               const uint32_t acc = (first && ks == 0 && k == 0) ? 0u : 1u;
               const uint64_t adesc = sdesc_sw128(sb + k * 32, 0, 1024);
               mma_bf16_pair(tmem, adesc, sdesc_sw128(sb + 16384 + k * 2048, 8192, 1024), id0, acc);
-              if (n_mma == 2) mma_bf16_pair(tmem + 256, adesc, sdesc_sw128(sb + e1_off + k * 2048, 8192, 1024), id1, acc);
             }
             mma_commit_pair_mc(smem_addr(&bar_empty2[stage]), 3);
             if (++stage == n_stages_c) { stage = 0; ph ^= 1; }
@@ -977,9 +930,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       p.az[(size_t)i * p.n_a + slot] = z_run;
       if (ovf) p.overflow[i] = 1;
     }
-    // Consume phase: warp w reads accumulator m = hc (columns d0 + 256m ...) for its lane quarter.
-    const int m = hc;
-    if (!is_a && m < n_mma) {
+    // Consume phase: the warps of id half hc read columns [hc N0/2, (hc + 1) N0/2) of the
+    // accumulator for their lane quarter.
+    if (!is_a) {
       bool have = n_cons > 0 && ok;
       if (n_cons > 0) {
         bool got = wait_bar(smem_addr(&bar_tfull[1]), 0, p);
@@ -988,15 +941,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
       }
       have = __all_sync(0xffffffffu, have);
-      const int Nm = m ? N1 : N0;
       const int cend = d0 + nd;
       float* dst = p.cpart + ((size_t)ra * 256 + i) * p.d;
       float* dz = rb >= 0 ? p.cpart + ((size_t)rb * 256 + i) * p.d : nullptr;
-      for (int cc = 0; cc < Nm / 32; ++cc) {
-        const int col = d0 + m * 256 + cc * 32;
+      for (int cc = hc * (N0 / 64); cc < (hc + 1) * (N0 / 64); ++cc) {
+        const int col = d0 + cc * 32;
         float v[32];
         if (have) {
-          tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + m * 256 + cc * 32, v);
+          tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + cc * 32, v);
         } else {
 #pragma unroll
           for (int e = 0; e < 32; ++e) v[e] = 0.f;
@@ -1245,12 +1197,9 @@ bool make_pair_plan(int V, int d, PairPlan* q) {
   static const char* single = getenv("DG_VOCAB_SINGLE_SM");
   if (single && single[0] == '1') return false;
   const int pairs = pair_capacity() < num_sms() / 2 ? pair_capacity() : num_sms() / 2;
-  // consumer slice width: 256 columns (one MMA of N = 256 per k-slice); 512
-  // (two MMAs sharing the P operand) measured 0.5-1% slower at d = 2816 and is
-  // kept behind DG_VOCAB_CW=512
-  static const int cw_env = env_int("DG_VOCAB_CW", 256);
-  static const int ks_env = env_int("DG_VOCAB_KSPLIT", 0);
-  q->cw = cw_env == 512 ? 512 : 256;
+  // consumer slice width: 256 columns (one MMA of N = 256 per k-slice; 512 columns, two MMAs
+  // sharing the P operand, measured 0.5-1% slower at d = 2816)
+  q->cw = 256;
   q->n_vt = (V + kVT - 1) / kVT;
   q->n_full = d / q->cw;
   q->rem = d % q->cw;
@@ -1261,7 +1210,6 @@ bool make_pair_plan(int V, int d, PairPlan* q) {
   const double wmax = q->n_full > 0 ? (double)q->cw : (double)q->rem;
   double best = -1.0;
   for (int ks = 1; ks <= 32 && ks <= q->n_vt; ++ks) {
-    if (ks_env && ks != ks_env) continue;
     const int n_pc = ks * q->n_fullx + (half ? (ks + 1) / 2 : 0);
     if (n_pc >= pairs) break;
     const int n_pa = pairs - n_pc < q->n_vt ? pairs - n_pc : q->n_vt;
@@ -1288,7 +1236,6 @@ Plan as_plan(const PairPlan& q) {
   p.n_a = 2 * (q.n_pa + q.n_pc);  // statistics slots: (pair, id half); every pair produces a tile
   p.n_c = 2 * q.n_pc;
   p.n_dt = 0;
-  p.window = 1 << 30;
   return p;
 }
 
@@ -1347,7 +1294,6 @@ int vocab_tc_launch(const __nv_bfloat16* h, const __nv_bfloat16* emb, int C, int
   Params p;
   p.C = C; p.V = V; p.d = d;
   p.n_rh = pl.n_rh; p.n_dt = pl.n_dt; p.n_vt = pl.n_vt; p.ksplit = pl.ksplit; p.n_a = pl.n_a;
-  p.window = pl.window;
   p.n_pa = pairs ? pq.n_pa : 0;
   p.n_pc = pairs ? pq.n_pc : 0;
   p.n_full = pairs ? pq.n_full : 0;
@@ -1355,24 +1301,36 @@ int vocab_tc_launch(const __nv_bfloat16* h, const __nv_bfloat16* emb, int C, int
   p.n_fullx = pairs ? pq.n_fullx : 0;
   p.cw = pairs ? pq.cw : 0;
   p.ring_bytes = kRingBytes;
-  // L2 eviction hints on by default (measured: DRAM reads 725 -> 601 MB at
-  // V=65536); DG_VOCAB_L2HINT=2 turns them off for comparison.
-  static const int l2hint = env_int("DG_VOCAB_L2HINT", 1);
-  p.l2hint = l2hint == 1;
-  // paired form: H and producer E evict_last, P and consumer E evict_first
-  // (DG_VOCAB_L2POL=dddd overrides, one digit per stream as in Params::pol)
-  static const char* pol_env = getenv("DG_VOCAB_L2POL");
-  for (int k = 0; k < 4; ++k) {
-    const int dflt = l2hint == 1 ? (k < 2 ? 1 : 2) : 0;
-    p.pol[k] = pol_env && strlen(pol_env) == 4 && pol_env[k] >= '0' && pol_env[k] <= '3' ? pol_env[k] - '0' : dflt;
+  if (pairs) {
+    // Large vocabularies: the consumer pairs' first-round tiles are the last ones (consumed last),
+    // so that consumers do not start with a backlog of a whole round; in steady state a consumer
+    // then reads a tile's E rows about one producer tile-time after the producer streamed them,
+    // more of them still in L2 (measured at V = 262144, d = 2816: DRAM reads 2.44 instead of
+    // 2.64 GB per call, same time). Small ones (fewer than four tiles per pair): consumer pair ci
+    // makes tile n_pa + ci, since there the deferred tiles would be consumed after everything
+    // else with nothing left to overlap them (V = 32768, d = 1024: 0.0609 against 0.0597 ms).
+    const int NP = pq.n_pa + pq.n_pc;
+    if (pl.n_vt >= 4 * NP) {
+      int n_def = pl.n_vt - pq.n_pa;
+      if (n_def > pq.n_pc) n_def = pq.n_pc;
+      if (n_def < 0) n_def = 0;
+      p.cb = pl.n_vt - n_def;
+      p.pb = pq.n_pa;
+      p.pe = pl.n_vt - n_def;
+    } else {
+      p.cb = pq.n_pa;
+      p.pb = NP;
+      p.pe = pl.n_vt;
+    }
+  } else {
+    p.cb = p.pb = p.pe = 0;
   }
   int* flags = (int*)(w + L.flags);
   p.ready = flags;
-  p.consumed = flags + pl.n_vt;
-  p.ref_count = flags + 2 * pl.n_vt;
-  p.abort_flag = flags + 2 * pl.n_vt + 1;
-  p.overflow = flags + 2 * pl.n_vt + 2;
-  p.rowkey = (unsigned*)(flags + 2 * pl.n_vt + 2 + 256);
+  p.ref_count = flags + pl.n_vt;
+  p.abort_flag = flags + pl.n_vt + 1;
+  p.overflow = flags + pl.n_vt + 2;
+  p.rowkey = (unsigned*)(flags + pl.n_vt + 2 + 256);
   p.smax = (float*)(w + L.smax);
   p.am = (float*)(w + L.am);
   p.aa = (int*)(w + L.aa);

@@ -5,10 +5,11 @@ dg_vocab_step_renoise, or their device-length forms inside the per-canvas
 CUDA graph), against the float64 oracle, step after step.
 
 Decisions (argmax, conf < threshold, re-noised tokens) must be identical
-except at positions the oracle flags (top-2 probability gap or
-|conf - threshold| below 1e-3, and, for argmax alone, a relative logit gap
-below 1e-3); flagged positions must stay below 0.5% of all positions x
-steps of the workload. Philox draws are bit-exact at every re-noised
+except at positions the oracle flags (top-2 probability gap at a kept
+position, or |conf - threshold|, below 1e-3); flagged positions must stay
+below 0.5% of all positions x steps of the workload. argmax is also compared
+where the token is a draw, flagged there by a relative logit gap below 1e-3,
+and may differ at no more than 0.5% of positions. Philox draws are bit-exact at every re-noised
 position, flagged or not. Floats: per-row relative 2e-2 (attention output,
 self-conditioning), 1e-2 absolute (log-sum-exp), 1e-2 relative (conf).
 
@@ -34,19 +35,23 @@ def _np(t):
 
 
 class Tally:
-    """Flagged positions over all positions x steps of one workload."""
+    """Flagged positions (decisions) and argmax differences over all positions
+    x steps of one workload."""
 
     def __init__(self):
         self.flagged = 0
+        self.am_diff = 0
         self.total = 0
 
-    def add(self, flags):
+    def add(self, flags, am_diff):
         self.flagged += int(np.count_nonzero(flags))
+        self.am_diff += int(np.count_nonzero(am_diff))
         self.total += flags.size
 
     def check(self):
         assert self.total > 0
         assert self.flagged <= FLAG_BUDGET * self.total, f"{self.flagged}/{self.total} positions flagged"
+        assert self.am_diff <= max(1, int(FLAG_BUDGET * self.total)), f"argmax differs at {self.am_diff} rows"
 
 
 def check_decisions(rv, thr, V, seed, step, pos0, tok, rn, am, tally, what):
@@ -64,7 +69,7 @@ def check_decisions(rv, thr, V, seed, step, pos0, tok, rn, am, tally, what):
     np.testing.assert_array_equal(tok[~low], am[~low], err_msg=f"{what}: kept positions")
     gap = logit_gap_flags(rv)
     assert ((am == rv["argmax"]) | fl | gap).all(), f"{what}: argmax differs at an unflagged row"
-    tally.add(fl | gap)
+    tally.add(fl, am != rv["argmax"])
 
 
 def check_stats(rv, conf, lse, what, sc=None):

@@ -310,7 +310,7 @@ def test_denoise_steps_match_oracle(lib, name):
     np.testing.assert_array_equal(_np(tokens), oracle.canvas_init(w.C, w.V, w.seed, w.prefix))
     tol = 1e-4 if dt == torch.float32 else 2e-2
     lse_tol = 1e-4 if dt == torch.float32 else LSE_ABS
-    flagged = total = 0
+    flagged = total = am_diff = 0
     for step in range(w.steps):
         q, kn, vn = synth.canvas_qkv(w.C, w.Hq, w.Hkv, w.hd, w.seed, step=step, dtype=dt)
         h = synth.hidden(emb, tgt, w.alpha, w.seed, step=step, dtype=dt)
@@ -329,8 +329,11 @@ def test_denoise_steps_match_oracle(lib, name):
         assert ((_np(am) == rv["argmax"]) | fl | gap).all()
         np.testing.assert_allclose(_np(conf), rv["conf"], rtol=1e-4 if dt == torch.float32 else CONF_REL)
         assert np.abs(_np(vl) - rv["lse"]).max() <= lse_tol
-        flagged += int((fl | gap).sum())
+        flagged += int(fl.sum())
+        am_diff += int((_np(am) != rv["argmax"]).sum())
         total += w.C
         assert_rows_close(_np(sc), rv["selfcond"], tol=tol)
+    # the budget covers decision flags; argmax (a diagnostic where the token is a draw) differs rarely
     assert flagged <= FLAG_BUDGET * total, f"{flagged}/{total} flagged"
+    assert am_diff <= max(1, int(FLAG_BUDGET * total)), f"argmax differs at {am_diff} rows"
     _status_ok()
