@@ -33,13 +33,15 @@
 // in TMEM leaves shared-memory bandwidth to the S operands and the TMA ring.
 //
 // Split merge (no second kernel; the launch is cooperative, so every CTA is
-// resident): each CTA writes its normalised O rows (bf16, piece-major so
-// that every warp store is 512 contiguous bytes) and per-row lse to its slot
-// of the workspace and arrives on its (row block, KV head) counter. Once all splits of the
-// group have arrived, CTA k merges rows [k*ceil(256/splits), ...) with
-// weights exp(lse_s - lse) and writes the bf16 output and the final lse. With
-// a single split the staged rows are the output: the launch is not
-// cooperative and the rows are copied straight out.
+// resident): CTA k of a (row block, KV head) group merges rows
+// [k*rpc, (k+1)*rpc), rpc = ceil(256/splits). Each CTA writes its normalised
+// O rows (bf16) and per-row lse into the workspace slices of the CTAs that
+// merge them ([split][16-byte piece][row in slice], so a warp's stores are
+// contiguous per piece) and arrives on the group's counter. Once all splits
+// have arrived, CTA k fetches its whole slice with one bulk copy into shared
+// memory and merges it with weights exp(lse_s - lse), writing the bf16 output
+// and the final lse. With a single split the staged rows are the output: the
+// launch is not cooperative and the rows are copied straight out.
 // Every wait is bounded (about two seconds); on expiry the CTA latches
 // DG_ERR_TIMEOUT, drains what it issued, frees TMEM and returns.
 #include <cudaTypedefs.h>
@@ -81,9 +83,13 @@ struct TcArgs {
   int64_t P;              // cache prefix (with P_dev: its upper bound)
   const int64_t* P_dev;   // device-side prefix length, or null
   int n_cache_tiles, n_tiles, tiles_per_split, splits;
-  uint4* part_o;    // [group][split][16 pieces][256 rows] x 8 bf16 (O / l)
-  float* part_lse;  // [group][split][256]
-  int* arrived;     // [group] splits that have published their partial (zeroed before launch)
+  // Partial results, per group one slice for each merging CTA k (rows [k rpc, k rpc + rpc) of the
+  // group): [split][16-byte piece][row in slice] (O / l, 8 bf16 each), then [split][row in slice]
+  // lse; slice_bytes apart, so a merging CTA fetches its slice with one bulk copy.
+  uint8_t* part;
+  int rpc;
+  uint32_t slice_bytes;
+  int* arrived;  // [group] splits that have published their partial (zeroed before launch)
   float scale_log2;
   int causal;
   int q_tma;  // Q tiles by TMA (the stacked rows of 128 / group positions form one box)
@@ -164,7 +170,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const __grid_constant__ CUtensorMap tk_n, const __grid_constant__ CUtensorMap tv_n,
                 const __grid_constant__ CUtensorMap tq, const TcArgs a) {
   extern __shared__ __align__(1024) uint8_t smem_dyn[];
-  __shared__ __align__(8) uint64_t ring_full[kRing], ring_empty[kRing], s_full[2], p_full[2], o_full[2], q_full, drain;
+  __shared__ __align__(8) uint64_t ring_full[kRing], ring_empty[kRing], s_full[2], p_full[2], o_full[2], q_full, drain,
+      mrg_full;
   __shared__ uint32_t tmem_slot;
   __shared__ int abort_flag;
   __shared__ float s_lse[kBM];                  // per-row lse of this CTA's partial (natural log)
@@ -231,6 +238,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(smem_addr(&q_full), 1);
     mbar_init(smem_addr(&drain), 1);
+    mbar_init(smem_addr(&mrg_full), 1);
     fence_mbar_init();
     if (a.q_tma && n > 0) {
       // Q tile qt = stacked rows [mblk*256 + qt*128, +128) = positions
@@ -488,23 +496,28 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int e = 0; e < kHD; ++e) o[e] = 0.f;
     }
-    uint4* po = a.splits > 1
-                    ? a.part_o + ((size_t)(g * gridDim.x + mblk) * a.splits + split) * (kBM * (kHD / 8)) + rt
-                    : nullptr;
+    // several splits: this row's pieces go to the slice of the CTA that merges it
+    const int ks = rt / a.rpc, rs = rt % a.rpc;
+    uint8_t* slice = a.splits > 1
+                         ? a.part + ((size_t)(g * gridDim.x + mblk) * a.splits + ks) * a.slice_bytes
+                         : nullptr;
+    uint4* po = slice ? reinterpret_cast<uint4*>(slice) + (size_t)split * 16 * a.rpc + rs : nullptr;
 #pragma unroll
     for (int pc = 0; pc < kHD / 8; ++pc) {
       const float* x = o + pc * 8;
       const uint4 w = make_uint4(pack2(x[0] * inv, x[1] * inv), pack2(x[2] * inv, x[3] * inv),
                                  pack2(x[4] * inv, x[5] * inv), pack2(x[6] * inv, x[7] * inv));
       if (po)
-        po[pc * kBM] = w;
+        po[pc * a.rpc] = w;
       else
         *reinterpret_cast<uint4*>(sm + stage_off(rt, pc)) = w;
     }
     const float lse_row = row_ok ? lse_v : -INFINITY;
     if (po) {
-      a.part_lse[((size_t)(g * gridDim.x + mblk) * a.splits + split) * kBM + rt] = lse_row;
-      __threadfence();  // this split's rows, before the arrival below
+      reinterpret_cast<float*>(slice + (size_t)a.splits * 16 * a.rpc * 16)[split * a.rpc + rs] = lse_row;
+      // this split's rows, before the arrival below; the merging CTA reads them with a bulk copy
+      fence_proxy_async_global();
+      __threadfence();
     } else {
       s_lse[rt] = lse_row;
     }
@@ -541,31 +554,39 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         __nanosleep(32);
       }
+      if (go) {
+        // this CTA's slice of every split's rows -> shared memory (the ring area; every MMA has
+        // completed), one bulk copy (async proxy, after the acquire above)
+        fence_proxy_async_global();
+        const uint8_t* src = a.part + ((size_t)grp_id * cs + split) * a.slice_bytes;
+        mbar_expect_tx(smem_addr(&mrg_full), a.slice_bytes);
+        bulk_load(sbase + kOffRing, src, a.slice_bytes, smem_addr(&mrg_full));
+      }
       s_go = go;
     }
     __syncthreads();
     merge = s_go;
+    if (merge) {
+      const bool got = wait_bar(smem_addr(&mrg_full), 0, ctl);
+      merge = __syncthreads_and(got);
+    }
   }
   if (merge) {
-    // Rows [r0, r0 + nr) of the group are merged by this CTA, two 16-byte
-    // pieces (16 columns) per item, so that one round of loads usually covers
-    // a thread's work: the item's lse values and pieces of up to 9 splits
-    // are loaded at once, then combined with weights exp(lse_s - max) (an
-    // online rescale joins further batches of 9 splits).
+    // Rows [r0, r0 + nr) of the group are merged by this CTA from its slice in shared memory, two
+    // 16-byte pieces (16 columns) per item: the lse values and pieces of every split, combined with
+    // weights exp(lse_s - max) (an online rescale joins batches of 9 splits).
     constexpr int kBatch = 9;
     constexpr int kItemsPerRow = kRowPieces / 2;
-    const int rpc = (kBM + cs - 1) / cs;
+    const int rpc = a.rpc;
     const int r0 = split * rpc;
     const int nr = max(0, min(kBM, r0 + rpc) - r0);
-    const float* pl = a.part_lse + (size_t)grp_id * cs * kBM;
-    const uint4* pg = a.part_o + (size_t)grp_id * cs * (kBM * kRowPieces);
+    const uint4* pg = reinterpret_cast<const uint4*>(sm + kOffRing);  // [split][piece][row in slice]
+    const float* pl = reinterpret_cast<const float*>(sm + kOffRing + (size_t)cs * 16 * rpc * 16);
     for (int item = tid; item < nr * kItemsPerRow; item += kThreads) {
       const int t = item / kItemsPerRow, pc = (item % kItemsPerRow) * 2;
       const int row = r0 + t;
       const int64_t R = (int64_t)mblk * kBM + row;
       if (R >= M) continue;
-      const uint4* src0 = pg + (size_t)pc * kBM + row;  // piece-major partial rows
-      const uint4* src1 = src0 + kBM;
       float acc[16];
 #pragma unroll
       for (int e = 0; e < 16; ++e) acc[e] = 0.f;
@@ -577,10 +598,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int u = 0; u < kBatch; ++u) {
           lv[u] = -INFINITY;
           if (s0 + u < cs) {
-            const size_t so = (size_t)(s0 + u) * (kBM * kRowPieces);
-            lv[u] = __ldcg(pl + (size_t)(s0 + u) * kBM + row);
-            x0[u] = __ldcg(src0 + so);
-            x1[u] = __ldcg(src1 + so);
+            const uint4* src0 = pg + ((size_t)(s0 + u) * 16 + pc) * rpc + t;
+            lv[u] = pl[(s0 + u) * rpc + t];
+            x0[u] = src0[0];
+            x1[u] = src0[rpc];
           }
         }
         float bm = m;
@@ -617,6 +638,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (pc == 0 && a.lse) a.lse[h * a.C + i] = tot > 0.f ? m + logf(tot) : -INFINITY;
     }
   }
+  // the bulk copy, if issued, has landed (bounded: nothing of this CTA in flight at exit)
+  if (cs > 1 && tid == 0 && s_go) drain_bar(smem_addr(&mrg_full), 0, ctl);
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);
@@ -694,28 +717,41 @@ void attn_tc_plan(int C, int Hq, int Hkv, int64_t P, int* splits, int* tiles_per
   *splits = (tiles + tps - 1) / tps;
 }
 
-// Workspace: per (row block, KV head) group and split, the staged bf16 O rows
-// and the row lse; then one arrival counter per group.
+// Workspace: one arrival counter per (row block, KV head) group (zeroed before
+// each launch), then per group one slice per merging CTA ([split][16-byte
+// piece][row in slice] O rows, then [split][row in slice] lse).
 struct TcLayout {
-  size_t part_o, part_lse, arrived, total;
+  size_t counters, part, total;
   int64_t groups;
+  int rpc;
+  uint32_t slice_bytes;
 };
-TcLayout tc_layout(int C, int Hq, int Hkv, int64_t P) {
-  const int splits = max_splits(C, Hq, Hkv, P);  // the plan's splits never exceed this
+uint32_t slice_bytes(int splits, int rpc) {
+  return (uint32_t)(((size_t)splits * 16 * rpc * 16 + (size_t)splits * rpc * sizeof(float) + 15) & ~(size_t)15);
+}
+TcLayout tc_layout(int C, int Hq, int Hkv, int splits) {
   TcLayout L;
   const int64_t M = (int64_t)(Hq / Hkv) * C;
   L.groups = ((M + kBM - 1) / kBM) * Hkv;
   auto al = [](size_t x) { return (x + 255) & ~(size_t)255; };
-  L.part_o = 0;
-  L.part_lse = al((size_t)L.groups * splits * kBM * kHD * sizeof(__nv_bfloat16));
-  L.arrived = L.part_lse + al((size_t)L.groups * splits * kBM * sizeof(float));
-  L.total = splits > 1 ? L.arrived + al((size_t)L.groups * sizeof(int)) : 0;  // one split: no partials
+  L.rpc = (kBM + splits - 1) / splits;
+  L.slice_bytes = slice_bytes(splits, L.rpc);
+  L.counters = 0;
+  L.part = L.counters + al((size_t)L.groups * sizeof(int));
+  L.total = splits > 1 ? L.part + al((size_t)L.groups * splits * L.slice_bytes) : 0;  // one split: nothing
   return L;
 }
 
+// Sized for every split count up to the plan's bound (non-decreasing in P), so a workspace sized
+// for the largest prefix serves every smaller one.
 size_t attn_tc_workspace(int C, int Hq, int Hkv, int64_t P) {
   if (C < 1 || Hkv < 1 || Hq % Hkv) return 0;
-  return tc_layout(C, Hq, Hkv, P).total;
+  size_t need = 0;
+  for (int sp = 2; sp <= max_splits(C, Hq, Hkv, P); ++sp) {
+    const size_t t = tc_layout(C, Hq, Hkv, sp).total;
+    if (t > need) need = t;
+  }
+  return need;
 }
 
 int attn_tc_launch(const void* q, const void* k_cache, const void* v_cache, int64_t cap, int64_t P,
@@ -724,7 +760,7 @@ int attn_tc_launch(const void* q, const void* k_cache, const void* v_cache, int6
   DG_CUDA_TRY(prepare_kernel());
   int splits, tps;
   attn_tc_plan(C, Hq, Hkv, P, &splits, &tps);
-  const TcLayout L = tc_layout(C, Hq, Hkv, P);
+  const TcLayout L = tc_layout(C, Hq, Hkv, splits);
   if (splits > 1 && (!ws || ws_bytes < L.total || ((uintptr_t)ws & 255u))) return DG_ERR_WORKSPACE;
   int* st = status_ptr();
   if (!st) return DG_ERR_CUDA;
@@ -752,9 +788,10 @@ int attn_tc_launch(const void* q, const void* k_cache, const void* v_cache, int6
   a.n_tiles = a.n_cache_tiles + (C + kBN - 1) / kBN;
   a.tiles_per_split = tps;
   a.splits = splits;
-  a.part_o = splits > 1 ? (uint4*)((char*)ws + L.part_o) : nullptr;
-  a.part_lse = splits > 1 ? (float*)((char*)ws + L.part_lse) : nullptr;
-  a.arrived = splits > 1 ? (int*)((char*)ws + L.arrived) : nullptr;
+  a.part = splits > 1 ? (uint8_t*)ws + L.part : nullptr;
+  a.rpc = L.rpc;
+  a.slice_bytes = L.slice_bytes;
+  a.arrived = splits > 1 ? (int*)((char*)ws + L.counters) : nullptr;
   a.scale_log2 = scale * 1.4426950408889634f;
   a.causal = mask == DG_MASK_CAUSAL_BLOCK;
   a.q_tma = q_tma;

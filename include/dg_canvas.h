@@ -105,9 +105,9 @@ DG_API int dg_canvas_attn(const void* q, const void* k_cache, const void* v_cach
                    int C, int Hq, int Hkv, int hd, float scale, int dtype, int mask,
                    void* workspace, size_t workspace_bytes, void* stream);
 
-/* Canvas attention for callers that cannot allocate device memory (code
- * running during stream capture, hosts that own every device allocation,
- * plugins given no scratch buffer). The explainer pages have no counterpart:
+/* Canvas attention for callers that cannot allocate device memory (hosts that
+ * own every device allocation, plugins given no scratch buffer, loops where an
+ * allocation could synchronise the device). The explainer pages have no counterpart:
  * this is a deployment variant of dg_canvas_attn, same arguments and results
  * minus the workspace. Its split-KV scratch is a fixed array inside the
  * library's device image (dg_canvas_attn_noalloc_max_scratch() bytes, 32 MiB),
@@ -130,7 +130,13 @@ DG_API size_t dg_canvas_attn_noalloc_max_scratch(void);
  *   conf[i]    = softmax(l_i)[argmax[i]] = 1 / sum_v exp(l_iv - max l_i)
  *   lse[i]     = log-sum-exp of l_i (natural log)
  *   selfcond[i]= softmax(l_i) . emb     (the self-conditioning vector)
- * One streaming pass over vocabulary tiles; the logits never reach memory.
+ * One pass over vocabulary tiles of 256 ids. The fp32 logits never reach
+ * memory; the softmax numerators exp(l - R) (R a per-row reference) go to
+ * the workspace in bf16 (V x 512 bytes, read back through L2) for the
+ * self-conditioning product. E is streamed from HBM once for the logits;
+ * the self-conditioning product reads each E tile again shortly after, from
+ * L2 where it is still resident (measured at V = 262144, d = 2816: 2.3 GB of
+ * DRAM reads per call for a 1.48 GB table).
  *
  *   h        [C][d] (dtype)     emb [V][d] (dtype)
  *   argmax   [C] int32          conf [C] fp32      lse [C] fp32 or NULL
@@ -253,8 +259,10 @@ DG_API int dg_count_flags(const uint8_t* flags, int C, int32_t* count, void* str
  * lie in [0, prefix_max] (prefix_max <= cap; outside: clamped, and
  * DG_ERR_DEVICE_BOUNDS latched). The kernel is planned for prefix_max, so the
  * workspace is dg_canvas_attn_workspace_size(C, Hq, Hkv, hd, prefix_max, dtype).
- * Cache rows [P, prefix_max) are read and masked out: they must hold finite
- * values (zero-initialise the cache once). DG_BF16 and hd == 128 only.
+ * The key tiles follow the device-side P: no tile past P is read, except the
+ * rows past P inside the last, partly filled 128-row cache tile, which are
+ * read and masked out; they must hold finite values (zero-initialise the
+ * cache once). DG_BF16 and hd == 128 only.
  */
 DG_API int dg_canvas_attn_devlen(const void* q, const void* k_cache, const void* v_cache, int64_t cap,
                                  const int64_t* prefix_len_dev, int64_t prefix_max, const void* k_canvas,
