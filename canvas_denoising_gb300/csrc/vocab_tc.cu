@@ -27,7 +27,9 @@
 //      keep per-row running max / first argmax / sum of exp(l - R), and
 //      write P = exp(l - R) in bf16 to a global ring, already in the
 //      128-byte-swizzled K-major layout an MMA operand needs, then publish
-//      the tile with a release flag.
+//      the tile with a release flag. (Paired form: each warp assembles its
+//      rows in a 4 KB shared-memory stage, so the ring is written in whole
+//      128-byte lines.)
 //    - consumers own a slice of S's columns and a residue class of
 //      vocabulary tiles. GEMM2: S_slice += P_tile . E_tile[:, slice] with E
 //      read MN-major (the rows producers just streamed, mostly from L2),
@@ -41,7 +43,13 @@
 //    - vocab_main: one CTA per role unit (cta_group::1), M = 128 MMAs for
 //      each row half; used where two-CTA clusters cannot be placed.
 //  * A combine kernel merges producer statistics (max, lowest argmax, sums)
-//    and consumer partials into argmax, conf, lse and S (bf16).
+//    and consumer partials into argmax, conf, lse and S (bf16). After the
+//    paired form it is a programmatic dependent launch.
+//  * Cross-CTA hand-offs (reference count, tile flags): the CTA's threads
+//    write, meet at a barrier, and one thread publishes with a release
+//    add; the barrier orders the others' writes before that release, as in
+//    a cooperative grid sync. One thread polls, with acquire loads, and a
+//    barrier passes the outcome to the rest of the CTA.
 // Every wait is bounded (about two seconds of clock); on expiry the kernel
 // latches DG_ERR_TIMEOUT, raises a grid-wide abort flag, drains its own
 // copies and MMAs, frees TMEM and returns.
@@ -149,7 +157,7 @@ struct Params {
   int* abort_flag;
   int* overflow;   // [256]
   unsigned* rowkey;  // [256] paired form: running max of the sample, order-preserving key (0 = none)
-  float* smax;     // [256][n_a] sample maxima
+  float* smax;     // [256][n_a] sample maxima (vocab_main; the paired form has rowkey)
   float* am;       // [256][n_a] running max
   int* aa;         // [256][n_a] first argmax
   float* az;       // [256][n_a] sum of exp(l - R)
@@ -604,6 +612,12 @@ constexpr int kRingBytes = 196608;   // operand ring per CTA (6 producer stages;
 constexpr int kMaxRing = 6;
 constexpr uint32_t kStageA2 = 32768u;  // producer stage per CTA: H [128 x 64] + E [128 ids x 64]
 constexpr int kEpiWarps = 8;
+// Per epilogue warp, after the ring: 32 rows x 128 bytes. The warp builds a 4 KB block of P
+// (or 32 rows x 32 fp32 columns of its S partial) there and writes it to global memory in whole
+// lines. With each thread storing its own row (16-byte pieces 128 bytes apart across the warp)
+// a producer tile's exp-and-store pass took 3.3 instead of 2.3 us and the S partials 5 instead of
+// 3.5 us (V = 32768, d = 1024: 55.5 against 52.9 us per call).
+constexpr int kEpiStage = 4096;
 
 // d-slice and residue classes of consumer pair c: n_fullx slices per residue
 // class ra (n_full of cw columns, then possibly the remainder); pairs past
@@ -693,6 +707,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_alloc_pair(smem_addr(&tmem_slot), 512);
     tmem_relinquish_pair();
   }
+  // the combine kernel may be scheduled from now on (it waits for this grid's completion)
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   tc_fence_before();
   cluster_sync();  // both CTAs' barriers initialised and TMEM allocated
   tc_fence_after();
@@ -843,14 +859,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int i = (int)rank * 128 + r;
     const int slot = pair * 2 + hc;
     const uint32_t tl = tmem + ((uint32_t)(q * 32) << 16) + hc * 128;
+    uint8_t* stg = ring + p.ring_bytes + (warp - 2) * kEpiStage;  // this warp's 4 KB stage
     float R2 = 0.f, lim2 = 0.f;
     float m_run = -INFINITY, z_run = 0.f;
     int a_run = 0x7fffffff;
     bool ovf = false;
     bool ok = true;
     if (n_prod == 0) {
-      p.smax[(size_t)i * p.n_a + slot] = -INFINITY;
-      __threadfence();
       epi_sync();
       if (threadIdx.x == 64) red_release_add_gpu(p.ref_count, 1);
     }
@@ -883,12 +898,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (j == 0) {
         // this slot's first half-tile is its sample -> grid-wide reference: one
         // atomic max per row, read back once every CTA has contributed
-        p.smax[(size_t)i * p.n_a + slot] = cm;
         red_max_u32(p.rowkey + i, order_key(cm));
-        __threadfence();
+        // the barrier orders every thread's contribution before thread 64's release; thread 64
+        // alone polls for the other CTAs' and the barrier below passes the outcome on
         epi_sync();
-        if (threadIdx.x == 64) red_release_add_gpu(p.ref_count, 1);
-        const bool refd = wait_flag(p.ref_count, 2 * NP, p);
+        bool refd = true;
+        if (threadIdx.x == 64) {
+          red_release_add_gpu(p.ref_count, 1);
+          refd = wait_flag(p.ref_count, 2 * NP, p);
+        }
         if (epi_any(!refd)) { ok = false; break; }
         const float R = from_order_key(__ldcg(p.rowkey + i));
         R2 = R * kLog2e;
@@ -906,28 +924,38 @@ __global__ void __launch_bounds__(kThreads, 1)
       float zs[8];
 #pragma unroll
       for (int e = 0; e < 8; ++e) zs[e] = 0.f;
-      // P blocks [t][sub-tile of 64 ids][row half = rank], pre-swizzled K-major
-      uint8_t* prow = p.pbuf + ((size_t)((t * 4 + hc * 2) * 2 + (int)rank)) * kTileBytes + (size_t)r * 128;
+      // P blocks [t][sub-tile of 64 ids][row half = rank], pre-swizzled K-major. The warp's 32
+      // rows of a block are 4 KB of contiguous memory: each row's 128 bytes are built in the
+      // warp's shared-memory stage in their final (swizzled) order, then the 4 KB go out in
+      // 512-byte coalesced stores.
 #pragma unroll
-      for (int e8 = 0; e8 < 16; ++e8) {
-        float pe[8];
+      for (int sub = 0; sub < 2; ++sub) {
 #pragma unroll
-        for (int f = 0; f < 8; f += 2) {
-          float x0, x1;
-          fma2(x0, x1, v[e8 * 8 + f], v[e8 * 8 + f + 1], kLog2e, kLog2e, -R2, -R2);
-          pe[f] = ex2_approx(x0);  // masked ids: exp2(-inf) = 0
-          pe[f + 1] = ex2_approx(x1);
-          add2(zs[f], zs[f + 1], pe[f], pe[f + 1]);
+        for (int piece = 0; piece < 8; ++piece) {
+          const int e8 = sub * 8 + piece;
+          float pe[8];
+#pragma unroll
+          for (int f = 0; f < 8; f += 2) {
+            float x0, x1;
+            fma2(x0, x1, v[e8 * 8 + f], v[e8 * 8 + f + 1], kLog2e, kLog2e, -R2, -R2);
+            pe[f] = ex2_approx(x0);  // masked ids: exp2(-inf) = 0
+            pe[f + 1] = ex2_approx(x1);
+            add2(zs[f], zs[f + 1], pe[f], pe[f + 1]);
+          }
+          *reinterpret_cast<uint4*>(stg + lane * 128 + ((piece ^ (lane & 7)) << 4)) =
+              make_uint4(pack2(pe[0], pe[1]), pack2(pe[2], pe[3]), pack2(pe[4], pe[5]), pack2(pe[6], pe[7]));
         }
-        const int sub = e8 >> 3, piece = e8 & 7;
-        uint8_t* dst = prow + (size_t)sub * 2 * kTileBytes + ((piece ^ (r & 7)) << 4);
-        *reinterpret_cast<uint4*>(dst) =
-            make_uint4(pack2(pe[0], pe[1]), pack2(pe[2], pe[3]), pack2(pe[4], pe[5]), pack2(pe[6], pe[7]));
+        __syncwarp();
+        uint8_t* blk = p.pbuf + ((size_t)((t * 4 + hc * 2 + sub) * 2 + (int)rank)) * kTileBytes + (size_t)q * 4096;
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+          *reinterpret_cast<uint4*>(blk + k * 512 + lane * 16) =
+              *reinterpret_cast<const uint4*>(stg + k * 512 + lane * 16);
+        __syncwarp();
       }
       z_run += ((zs[0] + zs[1]) + (zs[2] + zs[3])) + ((zs[4] + zs[5]) + (zs[6] + zs[7]));
       // publish this CTA's half of the P tile (consumers wait for both halves)
       fence_proxy_async_global();
-      __threadfence();
       epi_sync();
       if (threadIdx.x == 64 && !(p.inject && t == 0)) red_release_add_gpu(p.ready + t, 1);
     }
@@ -949,8 +977,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       have = __all_sync(0xffffffffu, have);
       const int cend = d0 + nd;
-      float* dst = p.cpart + ((size_t)ra * 256 + i) * p.d;
-      float* dz = rb >= 0 ? p.cpart + ((size_t)rb * 256 + i) * p.d : nullptr;
+      // Each thread holds 32 columns of its row; through the warp's stage, 8 lanes then
+      // write each row's 128 bytes together (4 rows per store instruction).
+      const int rr0 = lane >> 3, pc = lane & 7;
       for (int cc = hc * (N0 / 64); cc < (hc + 1) * (N0 / 64); ++cc) {
         const int col = d0 + cc * 32;
         float v[32];
@@ -960,13 +989,25 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int e = 0; e < 32; ++e) v[e] = 0.f;
         }
-        if (i < p.C && col < cend) {
+        if (col >= cend) continue;  // warp-uniform
 #pragma unroll
-          for (int e = 0; e < 32; e += 4) {
-            *reinterpret_cast<float4*>(dst + col + e) = make_float4(v[e], v[e + 1], v[e + 2], v[e + 3]);
-            if (dz) *reinterpret_cast<float4*>(dz + col + e) = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int e4 = 0; e4 < 8; ++e4)
+          *reinterpret_cast<float4*>(stg + lane * 128 + ((e4 ^ (lane & 7)) << 4)) =
+              make_float4(v[4 * e4], v[4 * e4 + 1], v[4 * e4 + 2], v[4 * e4 + 3]);
+        __syncwarp();
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const int rr = 4 * k + rr0;
+          const int ir = (int)rank * 128 + q * 32 + rr;
+          if (ir < p.C) {
+            const float4 x = *reinterpret_cast<const float4*>(stg + rr * 128 + ((pc ^ (rr & 7)) << 4));
+            *reinterpret_cast<float4*>(p.cpart + ((size_t)ra * 256 + ir) * p.d + col + 4 * pc) = x;
+            if (rb >= 0)
+              *reinterpret_cast<float4*>(p.cpart + ((size_t)rb * 256 + ir) * p.d + col + 4 * pc) =
+                  make_float4(0.f, 0.f, 0.f, 0.f);
           }
         }
+        __syncwarp();
       }
     }
   }
@@ -993,19 +1034,26 @@ __global__ void __launch_bounds__(kThreads, 1)
 // producers is recomputed here from scratch with its true maximum as the
 // reference (fp32, CUDA cores; slow, only for rows whose logits exceed the
 // sampled reference by more than the safe margin).
+// kMaxSplitRegs: residue classes whose partials a thread holds in registers
+// (8: 64 registers, four CTAs per SM; 16, for small d_model where the plan
+// takes up to 16 classes: 128 registers, two CTAs per SM). Launched after the
+// paired kernel as a programmatic dependent, so that its launch overlaps that
+// kernel's last CTAs; griddepcontrol.wait returns once the paired kernel has
+// completed and its writes are visible (at once after vocab_main).
 constexpr int kCombineCols = 1024;  // columns of S per combine CTA (4 per thread)
 
-__global__ void __launch_bounds__(256) vocab_combine(const Params p, const __nv_bfloat16* __restrict__ h,
-                                                     const __nv_bfloat16* __restrict__ emb, int32_t* argmax,
-                                                     float* conf, float* lse, __nv_bfloat16* selfcond) {
+template <int kMaxSplitRegs, int kMinBlocks>
+__global__ void __launch_bounds__(256, kMinBlocks)
+    vocab_combine(const Params p, const __nv_bfloat16* __restrict__ h, const __nv_bfloat16* __restrict__ emb,
+                  int32_t* argmax, float* conf, float* lse, __nv_bfloat16* selfcond) {
   extern __shared__ float hrow[];  // [d] (recompute path only)
   __shared__ float s_m[8], s_z[8], s_r[8], s_pv[256];
   __shared__ int s_a[8];
   const int i = blockIdx.x, slice = blockIdx.y, t = threadIdx.x, lane = t & 31, w = t >> 5;
+  asm volatile("griddepcontrol.wait;" ::: "memory");
 
   // Issue this thread's partial-S loads first (4 columns x every split), so
   // they are in flight while the row statistics are reduced below.
-  constexpr int kMaxSplitRegs = 8;
   const int jc = slice * kCombineCols + 4 * t;
   const bool has_cols = selfcond && jc < p.d && p.ksplit <= kMaxSplitRegs;
   float4 part[kMaxSplitRegs];
@@ -1017,6 +1065,7 @@ __global__ void __launch_bounds__(256) vocab_combine(const Params p, const __nv_
       if (k < p.ksplit) part[k] = __ldcg(reinterpret_cast<const float4*>(src + k * kstride));
   }
   const bool ovf = __ldcg(p.overflow + i) != 0;  // with the loads above, not after the reductions
+  const unsigned rkey = p.n_pa > 0 ? __ldcg(p.rowkey + i) : 0u;
   float m = -INFINITY, z = 0.f, R = -INFINITY;
   int ai = 0x7fffffff;
   const size_t rb = (size_t)i * p.n_a;
@@ -1024,7 +1073,7 @@ __global__ void __launch_bounds__(256) vocab_combine(const Params p, const __nv_
     const float ma = p.am[rb + a];
     const int aa = p.aa[rb + a];
     z += p.az[rb + a];
-    R = fmaxf(R, p.smax[rb + a]);
+    if (p.n_pa == 0) R = fmaxf(R, p.smax[rb + a]);
     if (ma > m || (ma == m && aa < ai)) { m = ma; ai = aa; }
   }
   for (int o = 16; o; o >>= 1) {
@@ -1034,6 +1083,7 @@ __global__ void __launch_bounds__(256) vocab_combine(const Params p, const __nv_
     z += __shfl_xor_sync(0xffffffffu, z, o);
     R = fmaxf(R, __shfl_xor_sync(0xffffffffu, R, o));
   }
+  if (p.n_pa > 0) R = from_order_key(rkey);
   if (lane == 0) { s_m[w] = m; s_a[w] = ai; s_z[w] = z; s_r[w] = R; }
   __syncthreads();
   m = s_m[0]; ai = s_a[0]; z = s_z[0]; R = s_r[0];
@@ -1157,7 +1207,7 @@ int pair_capacity() {
       cap = num_sms() / 2;
       return;
     }
-    const size_t smem = (size_t)kRingBytes + 1024;
+    const size_t smem = (size_t)kRingBytes + kEpiWarps * kEpiStage + 1024;
     if (cudaFuncSetAttribute(vocab_pair, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess) {
       cudaGetLastError();
       return;
@@ -1188,18 +1238,41 @@ struct PairPlan {
 };
 
 // Splits the pairs between the roles and picks the number of vocabulary residue
-// classes (ksplit) that maximises the tile rate, in units of one producer
-// pair's rate: producers give n_pa; a consumer pair of width w does w/d of a
-// producer pair's work per tile at kConsumerRate of its speed, so the residue
-// classes sustain kConsumerRate * ksplit * d / w (remainder pairs, serving two
-// classes, kConsumerRate * ksplit * d / (2 rem)). False if no split fits.
+// classes (ksplit) that minimises the step's length, in units of one producer
+// pair's tile time. In the first round every pair makes one tile; the
+// producer pairs then make the remaining n_vt - (n_pa + n_pc) tiles in
+// ceil(remaining / n_pa) rounds. A consumer pair of width w takes each of the
+// ceil(n_vt / ksplit) tiles of its class in w / d of a producer tile's time at
+// `rate` of its speed (remainder pairs, serving two classes, 2 ceil(n_vt /
+// ksplit) tiles of width rem). The length is the larger of the two; ties go to
+// the higher steady-state tile rate min(n_pa, rate ksplit d / w). False if no
+// split fits.
 //
-// kConsumerRate is measured, not derived: consumers start one producer tile
-// late, receive tiles in bursts and finish after the last one is published.
-// At V = 262144, d = 2816 (512-column slices) the step took 0.597 / 0.536 /
-// 0.598 ms with 37 / 32 / 26 producer pairs, and with 256-column slices
-// 0.651 / 0.536 / 0.704 ms with 43 / 32 / 26; 0.73 makes the plan pick 32.
+// The consumer rate is measured, not derived. With a table larger than L2 a
+// consumer re-reads a share of its E rows from DRAM and runs at 0.73 of the
+// MMA rate: at V = 262144, d = 2816 (512-column slices) the step took 0.597 /
+// 0.536 / 0.598 ms with 37 / 32 / 26 producer pairs, and with 256-column
+// slices 0.651 / 0.536 / 0.704 ms with 43 / 32 / 26. A table that fits in L2
+// is re-read from there and consumers run at the full rate: at V = 32768,
+// d = 1024 the step took 49.3 / 47.2 / 46.8 / 45.2 / 45.9 / 46.7 us with 9-14
+// residue classes, the model's order (12 first).
 constexpr double kConsumerRate = 0.73;
+
+size_t l2_bytes() {
+  static size_t n = 0;
+  if (!n) {
+    int dev = 0, v = 0;
+    if (cudaGetDevice(&dev) == cudaSuccess && cudaDeviceGetAttribute(&v, cudaDevAttrL2CacheSize, dev) == cudaSuccess &&
+        v > 0)
+      n = (size_t)v;
+    else {
+      cudaGetLastError();
+      n = (size_t)126 << 20;  // no device: the GB300's L2
+    }
+  }
+  return n;
+}
+
 bool make_pair_plan(int V, int d, PairPlan* q) {
   static const char* single = getenv("DG_VOCAB_SINGLE_SM");
   if (single && single[0] == '1') return false;
@@ -1215,23 +1288,34 @@ bool make_pair_plan(int V, int d, PairPlan* q) {
   const bool half = q->rem > 0 && q->rem <= q->cw / 2 && q->n_full > 0;
   q->n_fullx = q->n_full + (q->rem > 0 && !half ? 1 : 0);
   const double wmax = q->n_full > 0 ? (double)q->cw : (double)q->rem;
-  double best = -1.0;
+  const double rate = (double)V * d * 2.0 <= (double)l2_bytes() ? 1.0 : kConsumerRate;
+  double best_len = 1e300, best_rate = -1.0;
   for (int ks = 1; ks <= 32 && ks <= q->n_vt; ++ks) {
     const int n_pc = ks * q->n_fullx + (half ? (ks + 1) / 2 : 0);
     if (n_pc >= pairs) break;
     const int n_pa = pairs - n_pc < q->n_vt ? pairs - n_pc : q->n_vt;
+    const int rest = q->n_vt - (n_pa + n_pc) > 0 ? q->n_vt - (n_pa + n_pc) : 0;
+    const int per_class = (q->n_vt + ks - 1) / ks;
+    double len = (double)((rest + n_pa - 1) / n_pa);
     double cons = 1e30;
-    if (q->n_fullx > 0) cons = fmin(cons, kConsumerRate * ks * (double)d / wmax);
-    if (half) cons = fmin(cons, kConsumerRate * ks * (double)d / (2.0 * q->rem));
-    const double rate = fmin((double)n_pa, cons);
-    if (rate > best + 1e-9) {
-      best = rate;
+    if (q->n_fullx > 0) {
+      len = fmax(len, per_class * wmax / d / rate);
+      cons = fmin(cons, rate * ks * (double)d / wmax);
+    }
+    if (half) {
+      len = fmax(len, 2.0 * per_class * q->rem / d / rate);
+      cons = fmin(cons, rate * ks * (double)d / (2.0 * q->rem));
+    }
+    const double tile_rate = fmin((double)n_pa, cons);
+    if (len < best_len - 1e-9 || (len < best_len + 1e-9 && tile_rate > best_rate + 1e-9)) {
+      best_len = len;
+      best_rate = tile_rate;
       q->ksplit = ks;
       q->n_pc = n_pc;
       q->n_pa = n_pa;
     }
   }
-  return best > 0.0;
+  return best_rate > 0.0;
 }
 
 // The single-SM plan's fields that size the workspace, for the paired form.
@@ -1358,7 +1442,7 @@ int vocab_tc_launch(const __nv_bfloat16* h, const __nv_bfloat16* emb, int C, int
   DG_CUDA_TRY(cudaMemsetAsync(flags, 0, L.flag_bytes, s));
 
   if (pairs) {
-    const size_t psmem = (size_t)p.ring_bytes + 1024;  // attribute (the maximum) set by pair_capacity()
+    const size_t psmem = (size_t)p.ring_bytes + kEpiWarps * kEpiStage + 1024;  // attribute (the maximum) set by pair_capacity()
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(2 * (pq.n_pa + pq.n_pc));
     cfg.blockDim = dim3(kThreads);
@@ -1399,10 +1483,20 @@ int vocab_tc_launch(const __nv_bfloat16* h, const __nv_bfloat16* emb, int C, int
   DG_CUDA_TRY(cudaLaunchKernelEx(&cfg, vocab_main, tm_h, tm_ek, tm_emn, p));
   }
 
-  dim3 cgrid(C, (d + kCombineCols - 1) / kCombineCols);
-  const size_t csmem = (size_t)d * sizeof(float);
-  vocab_combine<<<cgrid, 256, csmem, s>>>(p, h, emb, argmax, conf, lse, selfcond);
-  DG_LAUNCH_CHECK();
+  cudaLaunchConfig_t ccfg = {};
+  ccfg.gridDim = dim3(C, (d + kCombineCols - 1) / kCombineCols);
+  ccfg.blockDim = dim3(256);
+  ccfg.dynamicSmemBytes = (size_t)d * sizeof(float);
+  ccfg.stream = s;
+  cudaLaunchAttribute cattr[1];
+  cattr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  cattr[0].val.programmaticStreamSerializationAllowed = 1;
+  ccfg.attrs = cattr;
+  ccfg.numAttrs = pairs ? 1 : 0;
+  if (p.ksplit <= 8)
+    DG_CUDA_TRY(cudaLaunchKernelEx(&ccfg, vocab_combine<8, 4>, p, h, emb, argmax, conf, lse, selfcond));
+  else
+    DG_CUDA_TRY(cudaLaunchKernelEx(&ccfg, vocab_combine<16, 2>, p, h, emb, argmax, conf, lse, selfcond));
   return DG_OK;
 }
 
