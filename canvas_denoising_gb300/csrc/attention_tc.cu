@@ -515,9 +515,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float lse_row = row_ok ? lse_v : -INFINITY;
     if (po) {
       reinterpret_cast<float*>(slice + (size_t)a.splits * 16 * a.rpc * 16)[split * a.rpc + rs] = lse_row;
-      // this split's rows, before the arrival below; the merging CTA reads them with a bulk copy
+      // this split's rows, before the arrival below (ordered by the barrier); the merging CTA reads
+      // them with a bulk copy
       fence_proxy_async_global();
-      __threadfence();
     } else {
       s_lse[rt] = lse_row;
     }
