@@ -7,8 +7,8 @@
 // The fp32 logits never reach memory: the softmax numerators exp(l - R) go
 // in bf16 through a global ring (V x 512 bytes) to the CTAs that form S. E
 // is streamed from HBM once for the logits; the S product reads each E tile
-// again shortly after, from L2 where it is still resident (at V = 262144,
-// d = 2816: 2.3 GB of DRAM reads per call for a 1.48 GB table).
+// again shortly after, from L2 where most of it is still resident (at V =
+// 262144, d = 2816: 2.1 GB of DRAM reads per call for a 1.48 GB table).
 //
 // Design.
 //  * Fixed per-row reference. softmax(l) = exp(l - R) / sum exp(l - R) for
@@ -20,7 +20,8 @@
 //    A row whose true maximum exceeds R_i + 40 (exp would leave the safe
 //    fp32 range) is flagged and recomputed exactly by the combine kernel
 //    with R = its true maximum.
-//  * Two roles, all co-resident (cooperative launch, one CTA per SM):
+//  * Two roles, all co-resident (one CTA per SM, the grid sized from the
+//    device's occupancy; vocab_main by cooperative launch):
 //    - producers make vocabulary tiles of 256 ids (round robin). GEMM1:
 //      logits[rows x 256] = H . E_tile^T, K-loop over d in steps of 64
 //      through a TMA ring. Eight epilogue warps read the logits from TMEM,
@@ -1455,11 +1456,14 @@ int vocab_tc_launch(const __nv_bfloat16* h, const __nv_bfloat16* emb, int C, int
     attr[1].val.clusterDim.x = 2;
     attr[1].val.clusterDim.y = 1;
     attr[1].val.clusterDim.z = 1;
-    // DG_VOCAB_NONCOOP=1 drops the cooperative attribute (for profilers that
-    // cannot co-schedule it; every cross-CTA wait is bounded either way)
-    static const int noncoop = env_int("DG_VOCAB_NONCOOP", 0);
-    cfg.attrs = noncoop == 1 ? attr + 1 : attr;
-    cfg.numAttrs = noncoop == 1 ? 1 : 2;
+    // The grid is sized from the device's cluster occupancy (one CTA per SM), so every CTA is
+    // resident at once on an otherwise idle GPU, and every cross-CTA wait is bounded. The
+    // cooperative attribute adds the driver's guarantee of co-scheduling next to other work on
+    // the device; it is opt-in (DG_VOCAB_COOP=1) because Nsight Compute cannot replay a
+    // cooperative launch of two-CTA clusters (it refuses the launch), and it measured no faster.
+    static const int coop = env_int("DG_VOCAB_COOP", 0);
+    cfg.attrs = coop == 1 ? attr : attr + 1;
+    cfg.numAttrs = coop == 1 ? 2 : 1;
     DG_CUDA_TRY(cudaLaunchKernelEx(&cfg, vocab_pair, tm_h, tm_ek, tm_emn, tm_p, p));
   } else {
   const size_t smem = (size_t)kStages * kStageBytes + 1024;

@@ -182,11 +182,13 @@ class GraphedBlockDiffusion:
         self.graph = None
         self.events = events  # optional per-step (attn start, attn end, vocab start, vocab end) timing events
         self.launches = 1 + 3 * steps + 2  # kernels per canvas: init, steps x (attention + vocab 2), append 2
-        # record=True: every step's tokens, flags and statistics are copied (device to device, inside
-        # the graph) into per-step history buffers, so a whole canvas can be inspected step by step
+        # record=True: the initial canvas and every step's tokens, flags and statistics are copied
+        # (device to device, inside the graph) into history buffers, so a whole canvas can be
+        # inspected step by step
         self.history = None
         if record:
             self.history = {
+                "init": torch.empty(C, dtype=torch.int32, device=dev),
                 "tokens": torch.empty((steps, C), dtype=torch.int32, device=dev),
                 "renoised": torch.empty((steps, C), dtype=torch.uint8, device=dev),
                 "argmax": torch.empty((steps, C), dtype=torch.int32, device=dev),
@@ -198,6 +200,9 @@ class GraphedBlockDiffusion:
     def _canvas(self):
         o, s_, ev = self.out, self.stream, self.events
         B.canvas_init_devpos(self.tokens, self.V, self.seed, self.len_dev, stream=s_)
+        if self.history is not None:
+            with torch.cuda.stream(s_):
+                self.history["init"].copy_(self.tokens)
         for s in range(self.steps):
             if ev is not None:
                 ev[s][0].record(s_)

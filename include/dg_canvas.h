@@ -135,8 +135,15 @@ DG_API size_t dg_canvas_attn_noalloc_max_scratch(void);
  * the workspace in bf16 (V x 512 bytes, read back through L2) for the
  * self-conditioning product. E is streamed from HBM once for the logits;
  * the self-conditioning product reads each E tile again shortly after, from
- * L2 where it is still resident (measured at V = 262144, d = 2816: 2.3 GB of
- * DRAM reads per call for a 1.48 GB table).
+ * L2 where most of it is still resident (measured at V = 262144, d = 2816:
+ * 2.1 GB of DRAM reads per call for a 1.48 GB table).
+ * The step runs one CTA on every SM, all resident at once, with bounded
+ * waits between them: run it when other kernels do not hold SMs for long
+ * (a wait that expires, after about two seconds, sets DG_ERR_TIMEOUT in the
+ * device status word and the call's outputs are not valid). Setting
+ * DG_VOCAB_COOP=1 in the environment makes it a cooperative launch, which
+ * the driver co-schedules next to other work (Nsight Compute cannot replay
+ * that form).
  *
  *   h        [C][d] (dtype)     emb [V][d] (dtype)
  *   argmax   [C] int32          conf [C] fp32      lse [C] fp32 or NULL

@@ -171,7 +171,9 @@ def test_long_context_threshold_sweep(lib):
 def test_multiblock_graphed_against_oracle(lib):
     """8 canvases x 24 steps from a 2048-token prefix through the per-canvas
     CUDA graph with the cache length on the device (prefix 2048 -> 4096).
-    Every step of every canvas: the Philox draw at each re-noised position
+    Every canvas's initial tokens (the device-position canvas init) against
+    the oracle's draws. Every step of every canvas: the Philox draw at each
+    re-noised position
     (bit-exact), the argmax at each kept one, and the flags equal conf <
     threshold. The first and last step of every canvas: tokens, flags, conf,
     lse and attention lse against the oracle over the cache as it stood; the
@@ -201,6 +203,8 @@ def test_multiblock_graphed_against_oracle(lib):
         stream.synchronize()
         P = P0 + b * w.C
         hist = {key: _np(t) for key, t in gb.history.items()}
+        np.testing.assert_array_equal(hist["init"], oracle.canvas_init(w.C, w.V, w.seed, P),
+                                      err_msg=f"canvas {b}: initial tokens")
         for s in range(steps):
             what = f"canvas {b} step {s}"
             tok, rn, am, conf = hist["tokens"][s], hist["renoised"][s], hist["argmax"][s], hist["conf"][s]
