@@ -91,6 +91,10 @@ __device__ __forceinline__ uint32_t ld_acquire_gpu(const int* p) {
 __device__ __forceinline__ void red_release_add_gpu(int* p, int v) {
   asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
+// A count that orders nothing (a hint another CTA polls).
+__device__ __forceinline__ void red_add_relaxed_gpu(int* p, int v) {
+  asm volatile("red.relaxed.gpu.global.add.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
 
 // ---------------------------------------------------------------- tcgen05
 __device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
