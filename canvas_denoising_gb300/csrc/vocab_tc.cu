@@ -8,7 +8,7 @@
 // in bf16 through a global ring (V x 512 bytes) to the CTAs that form S. E
 // is streamed from HBM once for the logits; the S product reads each E tile
 // again shortly after, from L2 where most of it is still resident (at V =
-// 262144, d = 2816: 2.1 GB of DRAM reads per call for a 1.48 GB table).
+// 262144, d = 2816: 1.76 GB of DRAM reads per call for a 1.48 GB table).
 //
 // Design.
 //  * Fixed per-row reference. softmax(l) = exp(l - R) / sum exp(l - R) for
