@@ -63,7 +63,7 @@ extern "C" {
 typedef enum {
   DG_OK = 0,
   DG_ERR_INVALID_ARG = -1,   /* null/misaligned pointer, bad size, len+C > cap ... */
-  DG_ERR_UNSUPPORTED = -2,   /* shape or dtype this build does not implement      */
+  DG_ERR_UNSUPPORTED = -2,   /* shape or dtype the library does not implement     */
   DG_ERR_WORKSPACE = -3,     /* workspace smaller than the size query returned    */
   DG_ERR_CUDA = -4,          /* a CUDA runtime call or launch failed              */
   DG_ERR_TIMEOUT = -5,       /* (device status) a bounded wait ran out            */
