@@ -134,13 +134,18 @@ struct Layout {
 };
 
 size_t up256(size_t x) { return (x + 255) & ~(size_t)255; }
+size_t tile_words(int n_vt) { return ((size_t)n_vt + 3) / 4; }
+constexpr size_t kFlagFixed = 4 + 4 + 256 + 1024;  // reference count, abort, overflow, row keys
 
 Layout make_layout(const Plan& p, int d) {
   Layout L;
   size_t o = 0;
   L.flags = o;
-  // tile flags, reference count, abort, overflow[256], row keys[256], consumed tile counts
-  L.flag_bytes = (size_t)(p.n_vt + 2 + 256 + 256 + p.n_vt) * sizeof(int);
+  // Flags, zeroed before each launch (bytes): tile published counts [n_vt] (a byte per tile in
+  // 32-bit words), reference count, abort, overflow [256] (a byte per row), row keys [256] (u32),
+  // then the pacing counts [n_vt] (bytes in words; zeroed only when pacing is on). Kept small: a
+  // memset of up to 4096 bytes costs ~1.2 us back to back, a larger one ~4.1 us.
+  L.flag_bytes = 2 * tile_words(p.n_vt) * 4 + kFlagFixed;
   o += up256(L.flag_bytes);
   L.smax = o; o += up256((size_t)p.n_a * 256 * 4);
   L.am = o;   o += up256((size_t)p.n_a * 256 * 4);
@@ -154,10 +159,10 @@ Layout make_layout(const Plan& p, int d) {
 
 struct Params {
   int C, V, d, n_rh, n_dt, n_vt, ksplit, n_a;
-  int* ready;      // [n_vt] tile published counters
+  unsigned* ready;  // tile published counts: tile t in byte t & 3 of word t >> 2
   int* ref_count;  // producers that have published their sample maxima
   int* abort_flag;
-  int* overflow;   // [256]
+  uint8_t* overflow;  // [256]
   unsigned* rowkey;  // [256] paired form: running max of the sample, order-preserving key (0 = none)
   float* smax;     // [256][n_a] sample maxima (vocab_main; the paired form has rowkey)
   float* am;       // [256][n_a] running max
@@ -186,7 +191,7 @@ struct Params {
   // paired form, pacing (lead > 0): a producer pair starts tile t (after its first) once the
   // consumer CTAs of tile t - lead have issued its loads (consumed[t - lead] == cons_per_tile), or
   // after pace_cycles: a soft wait that keeps the consumers' E re-reads within L2
-  int* consumed;
+  unsigned* consumed;  // tile t's count in byte t & 3 of word t >> 2
   int lead, cons_per_tile;
   long long pace_cycles;
 };
@@ -234,6 +239,35 @@ __device__ bool wait_flag(const int* flag, int target, const Params& p) {
   const long long t0 = clock64();
   for (uint32_t it = 0;; ++it) {
     if ((int)ld_acquire_gpu(flag) >= target) return true;
+    if (aborted(p.abort_flag)) return false;
+    if (clock64() - t0 > p.wait_cycles) {
+      raise_abort(p);
+      return false;
+    }
+    __nanosleep(64);
+  }
+}
+
+// Byte-per-tile counts in 32-bit words (every count stays below 256, and the word-wide adds below
+// 2^31, so lanes never carry into each other).
+__device__ __forceinline__ int tile_count(unsigned word, int t) { return (int)((word >> (8 * (t & 3))) & 0xffu); }
+__device__ __forceinline__ void tile_add_release(unsigned* w, int t) {
+  // word and lane computed inside the asm, where the compiler cannot hoist them into the loops
+  asm volatile(
+      "{\n .reg .u32 sh, v;\n .reg .u64 off, a;\n"
+      " and.b32 sh, %1, 3;\n shl.b32 sh, sh, 3;\n shl.b32 v, 1, sh;\n"
+      " shr.s32 sh, %1, 2;\n mul.wide.s32 off, sh, 4;\n add.u64 a, %0, off;\n"
+      " red.release.gpu.global.add.u32 [a], v;\n}"
+      ::"l"(w), "r"(t)
+      : "memory");
+}
+// Bounded acquire wait until tile t's count reaches target. An acquire that reads a later add to
+// the same word (another tile's) still synchronizes with this tile's release: adds extend the
+// release sequence.
+__device__ bool wait_tile(const unsigned* w, int t, int target, const Params& p) {
+  const long long t0 = clock64();
+  for (uint32_t it = 0;; ++it) {
+    if (tile_count(ld_acquire_gpu(reinterpret_cast<const int*>(w + (t >> 2))), t) >= target) return true;
     if (aborted(p.abort_flag)) return false;
     if (clock64() - t0 > p.wait_cycles) {
       raise_abort(p);
@@ -474,7 +508,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         fence_proxy_async_global();
         __threadfence();
         epi_sync();
-        if (threadIdx.x == 64 && !(p.inject && t == 0)) red_release_add_gpu(p.ready + t, 1);
+        if (threadIdx.x == 64 && !(p.inject && t == 0)) tile_add_release(p.ready, t);
       }
       if (active && i < p.C) {
         p.am[(size_t)i * p.n_a + a] = m_run;
@@ -505,7 +539,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool ok = true;
         for (int j = 0; j < n_my && ok; ++j) {
           const int t = kap + j * p.ksplit;
-          if (!wait_flag(p.ready + t, 1, p)) break;
+          if (!wait_tile(p.ready, t, 1, p)) break;
           fence_proxy_async_global();
           for (int ks = 0; ks < kVT / 64; ++ks) {
             if (!wait_bar(smem_addr(&bar_empty[stage]), ph ^ 1, p)) { ok = false; break; }
@@ -758,8 +792,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int t = prod_tile(p, pair, j);
           if (j > 0 && p.lead > 0 && t - p.lead >= 0) {
             const long long t0 = clock64();  // soft: never an error, only a delay of at most pace_cycles
-            while (*(volatile const int*)(p.consumed + t - p.lead) < p.cons_per_tile && !aborted(p.abort_flag) &&
-                   clock64() - t0 < p.pace_cycles)
+            const int tl = t - p.lead;
+            while (tile_count(*(volatile const unsigned*)(p.consumed + (tl >> 2)), tl) < p.cons_per_tile &&
+                   !aborted(p.abort_flag) && clock64() - t0 < p.pace_cycles)
               __nanosleep(256);
           }
           for (int ks = 0; ks < ksteps_d; ++ks) {
@@ -783,7 +818,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int u = 0; u < n_iter && ok; ++u) {
           const int t = consumer_tile(u, ra, rb, p.ksplit);
           if (t >= p.n_vt) continue;
-          if (!wait_flag(p.ready + t, 2, p)) break;
+          if (!wait_tile(p.ready, t, 2, p)) break;
           fence_proxy_async_global();
           for (int ks = 0; ks < kVT / 64; ++ks) {
             if (!wait_bar(smem_addr(&bar_empty2[stage]), ph ^ 1, p)) { ok = false; break; }
@@ -797,7 +832,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                                     t * kVT + ks * 64, fl, pol_e);
             if (++stage == n_stages_c) { stage = 0; ph ^= 1; }
           }
-          if (ok && p.lead > 0) red_add_relaxed_gpu(p.consumed + t, 1);  // pacing hint for the producers
+          if (ok && p.lead > 0)  // pacing hint for the producers
+            red_add_relaxed_gpu(reinterpret_cast<int*>(p.consumed + (t >> 2)), 1 << (8 * (t & 3)));
         }
       }
     }
@@ -972,7 +1008,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // publish this CTA's half of the P tile (consumers wait for both halves)
       fence_proxy_async_global();
       epi_sync();
-      if (threadIdx.x == 64 && !(p.inject && t == 0)) red_release_add_gpu(p.ready + t, 1);
+      if (threadIdx.x == 64 && !(p.inject && t == 0)) tile_add_release(p.ready, t);
     }
     if (i < p.C) {
       p.am[(size_t)i * p.n_a + slot] = m_run;
@@ -1432,12 +1468,13 @@ int vocab_tc_launch(const __nv_bfloat16* h, const __nv_bfloat16* emb, int C, int
     p.cb = p.pb = p.pe = 0;
   }
   int* flags = (int*)(w + L.flags);
-  p.ready = flags;
-  p.ref_count = flags + pl.n_vt;
-  p.abort_flag = flags + pl.n_vt + 1;
-  p.overflow = flags + pl.n_vt + 2;
-  p.rowkey = (unsigned*)(flags + pl.n_vt + 2 + 256);
-  p.consumed = flags + pl.n_vt + 2 + 512;
+  const size_t tw = tile_words(pl.n_vt);
+  p.ready = reinterpret_cast<unsigned*>(flags);
+  p.ref_count = flags + tw;
+  p.abort_flag = flags + tw + 1;
+  p.overflow = reinterpret_cast<uint8_t*>(flags + tw + 2);
+  p.rowkey = reinterpret_cast<unsigned*>(flags + tw + 2 + 64);
+  p.consumed = reinterpret_cast<unsigned*>(flags + tw + 2 + 64 + 256);
   p.lead = 0;
   p.cons_per_tile = 0;
   p.pace_cycles = 40000;  // ~20 us
@@ -1470,9 +1507,8 @@ int vocab_tc_launch(const __nv_bfloat16* h, const __nv_bfloat16* emb, int C, int
   const Inject inj = take_inject(kInjectVocabReady);
   p.inject = inj.kind != kInjectNone;
   p.wait_cycles = inj.wait_cycles > 0 ? inj.wait_cycles : kTimeoutCycles;
-  // the consumed counts are zeroed only when pacing reads them (a memset of 4 KB or less is also
-  // measurably cheaper: V = 65536, d = 2816, 3080 against 4104 bytes, 0.1456 against 0.1483 ms)
-  const size_t zero_bytes = L.flag_bytes - (p.lead > 0 ? 0 : (size_t)pl.n_vt * sizeof(int));
+  // the pacing counts are zeroed only when pacing reads them
+  const size_t zero_bytes = L.flag_bytes - (p.lead > 0 ? 0 : tw * 4);
   DG_CUDA_TRY(cudaMemsetAsync(flags, 0, zero_bytes, s));
 
   if (pairs) {
