@@ -201,8 +201,10 @@ class Canvas:
             ev[2].record(stream)
         B.canvas_attn(q, self.k, self.v, self.P, kn, vn, out=self.out, lse=self.lse_attn, workspace=self.ws_attn,
                       stream=stream)
-        # head_dim 128: one kernel (key splits merged in-kernel); otherwise + a combine when split
-        n += 1 if w.hd == 128 else (2 if self.ws_attn.numel() > 256 else 1)
+        # one attention kernel, plus (with key splits) a counter reset kernel ahead of it at
+        # head_dim 128 (DG_ATTN_COOP=1: a memset instead) or a combine kernel after it otherwise
+        split = self.ws_attn.numel() > 256
+        n += 2 if split and not (w.hd == 128 and os.environ.get("DG_ATTN_COOP") == "1") else 1
         if ev is not None and ev[3] is not None:
             ev[3].record(stream)
         if ev is not None and ev[0] is not None:
@@ -547,7 +549,7 @@ def run_ours(args, world, rank, local):
                  "traffic": committed_traffic("attn_fwd_tc", args.workload),
                  "peak_source": f"{pk['source']} bf16 burst", "algorithmic_flops_per_launch": aflops,
                  "avg_launch_ms": round(attn_ms, 4),
-                 "timing": "50 back-to-back calls right after the timed region (memset + kernel each), host ahead"}
+                 "timing": "50 back-to-back calls right after the timed region (counter reset + attention kernel each), host ahead"}
     steps_per_s = job_rate(world, K, ms)
     line = {
         "metric": metric_name(), "value": round(steps_per_s, 3), "unit": "steps/s", "n_gpus": world, "steps": K,

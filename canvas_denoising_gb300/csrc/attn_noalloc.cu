@@ -12,9 +12,9 @@
 // array: calls that can overlap on the GPU (different streams without
 // ordering between them) race on it and must not be issued. The contents left
 // by the previous call do not matter: the call zeroes the per-group arrival
-// counters it needs with a stream-ordered memset before its launch (the same
-// memset the workspace entry point issues), and every partial result is
-// written before it is read.
+// counters it needs, stream-ordered, before the attention kernel reads them
+// (the same reset the workspace entry point issues), and every partial result
+// is written before it is read.
 //
 // Host code cannot use the array's name as a device address (in host code it
 // names a host-side shadow). The device address is looked up with

@@ -24,6 +24,7 @@ part of this path; `backbone(block, step, tokens, selfcond)` supplies them
 """
 from __future__ import annotations
 
+import os
 from dataclasses import dataclass
 
 import torch
@@ -181,7 +182,12 @@ class GraphedBlockDiffusion:
                                     device=dev)
         self.graph = None
         self.events = events  # optional per-step (attn start, attn end, vocab start, vocab end) timing events
-        self.launches = 1 + 3 * steps + 2  # kernels per canvas: init, steps x (attention + vocab 2), append 2
+        # kernels per canvas: init, steps x (attention 1-2 + vocab 2), append 2; attention with key
+        # splits adds a counter reset kernel at head_dim 128 (DG_ATTN_COOP=1: a memset instead) and a
+        # combine kernel at other head dims
+        split = self.ws_attn.numel() > 256
+        n_attn = 2 if split and not (self.hd == 128 and os.environ.get("DG_ATTN_COOP") == "1") else 1
+        self.launches = 1 + (n_attn + 2) * steps + 2
         # record=True: the initial canvas and every step's tokens, flags and statistics are copied
         # (device to device, inside the graph) into history buffers, so a whole canvas can be
         # inspected step by step

@@ -98,6 +98,14 @@ DG_API int dg_device_status(void* stream);
  *   scale <= 0 selects 1/sqrt(hd). mask = dg_mask.
  * Requirements: Hq % Hkv == 0; hd in {32, 64, 128}; 0 <= P <= cap; C >= 1;
  * every pointer 16-byte aligned. Workspace: split-KV partials.
+ * At hd = 128 with key splits the call launches a one-CTA kernel that zeroes
+ * the workspace's arrival counters, then the attention kernel as its
+ * programmatic dependent: at most one CTA per SM, all resident at once, with
+ * bounded waits between the splits of a row block (a wait that expires,
+ * after about two seconds, sets DG_ERR_TIMEOUT and the outputs are not
+ * valid). DG_ATTN_COOP=1 in the environment replaces the reset kernel by a
+ * memset and makes the attention launch cooperative, which the driver
+ * co-schedules next to other work.
  */
 DG_API size_t dg_canvas_attn_workspace_size(int C, int Hq, int Hkv, int hd, int64_t prefix_len, int dtype);
 DG_API int dg_canvas_attn(const void* q, const void* k_cache, const void* v_cache, int64_t cap, int64_t prefix_len,
