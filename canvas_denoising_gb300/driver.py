@@ -182,12 +182,15 @@ class GraphedBlockDiffusion:
                                     device=dev)
         self.graph = None
         self.events = events  # optional per-step (attn start, attn end, vocab start, vocab end) timing events
-        # kernels per canvas: init, steps x (attention 1-2 + vocab 2), append 2; attention with key
+        # kernels per canvas: init, steps x (attention 1-2 + vocab 2-3), append 2; attention with key
         # splits adds a counter reset kernel at head_dim 128 (DG_ATTN_COOP=1: a memset instead) and a
-        # combine kernel at other head dims
+        # combine kernel at other head dims; the paired vocabulary form adds a flag reset kernel
+        # (DG_VOCAB_COOP=1: a memset instead)
         split = self.ws_attn.numel() > 256
         n_attn = 2 if split and not (self.hd == 128 and os.environ.get("DG_ATTN_COOP") == "1") else 1
-        self.launches = 1 + (n_attn + 2) * steps + 2
+        pairs = B.vocab_step_plan(C, self.V, self.d)["cluster_pairs"] > 0
+        n_vocab = 3 if pairs and os.environ.get("DG_VOCAB_COOP") != "1" else 2
+        self.launches = 1 + (n_attn + n_vocab) * steps + 2
         # record=True: the initial canvas and every step's tokens, flags and statistics are copied
         # (device to device, inside the graph) into history buffers, so a whole canvas can be
         # inspected step by step

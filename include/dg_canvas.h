@@ -148,10 +148,12 @@ DG_API size_t dg_canvas_attn_noalloc_max_scratch(void);
  * The step runs one CTA on every SM, all resident at once, with bounded
  * waits between them: run it when other kernels do not hold SMs for long
  * (a wait that expires, after about two seconds, sets DG_ERR_TIMEOUT in the
- * device status word and the call's outputs are not valid). Setting
- * DG_VOCAB_COOP=1 in the environment makes it a cooperative launch, which
- * the driver co-schedules next to other work (Nsight Compute cannot replay
- * that form).
+ * device status word and the call's outputs are not valid). A one-CTA
+ * kernel first zeroes the workspace's flags; the main kernel is launched as
+ * its programmatic dependent, and the combine kernel as the main kernel's.
+ * Setting DG_VOCAB_COOP=1 in the environment zeroes the flags with a memset
+ * and makes the main launch cooperative, which the driver co-schedules next
+ * to other work (Nsight Compute cannot replay that form).
  *
  *   h        [C][d] (dtype)     emb [V][d] (dtype)
  *   argmax   [C] int32          conf [C] fp32      lse [C] fp32 or NULL
