@@ -169,11 +169,14 @@ __device__ __forceinline__ float2 unpack2(uint32_t u) {
   return make_float2(__uint_as_float(u << 16), __uint_as_float(u & 0xFFFF0000u));
 }
 
-// The group arrival counters of the next attn_fwd_tc launch -> 0. It lets
-// its dependent launch start at once; the dependent's griddepcontrol.wait
-// returns after this grid has finished and its stores are visible.
+// The group arrival counters of the next attn_fwd_tc launch -> 0. It is
+// itself a programmatic dependent of whatever precedes it on the stream: it
+// lets its own dependent start at once, then waits for its predecessor to
+// finish before it writes. The dependent's griddepcontrol.wait returns after
+// this grid has finished and its stores are visible.
 __global__ void attn_zero_arrivals(int* arrived, int n) {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   for (int i = threadIdx.x; i < n; i += blockDim.x) arrived[i] = 0;
 }
 
@@ -826,8 +829,11 @@ int attn_tc_launch(const void* q, const void* k_cache, const void* v_cache, int6
   // Several splits meet on a counter, so every CTA must be resident: the grid
   // is one CTA per SM at most and every wait is bounded. By default the
   // counters are zeroed by attn_zero_arrivals and this launch is its
-  // programmatic dependent (18.5 vs 20.0 us per call measured at 16q/8kv
-  // heads, P = 4096; no change at P = 1024 or 32768). DG_ATTN_COOP=1 selects
+  // programmatic dependent (17.0 vs 20.0 us per call measured at 16q/8kv
+  // heads, P = 4096, back to back; no change at P = 1024 or 32768).
+  // attn_fwd_tc itself does not release its dependents early: a following
+  // vocabulary step whose CTAs were placed while attention still held the SMs
+  // ran slower (the whole step -2.5%). DG_ATTN_COOP=1 selects
   // a stream-ordered memset and a cooperative launch instead, which adds the
   // driver's guarantee of co-scheduling next to other work on the device.
   // Either way the counters start at zero on every call
@@ -851,8 +857,13 @@ int attn_tc_launch(const void* q, const void* k_cache, const void* v_cache, int6
     if (coop) {
       DG_CUDA_TRY(cudaMemsetAsync(a.arrived, 0, (size_t)L.groups * sizeof(int), s));
     } else {
-      attn_zero_arrivals<<<1, 64, 0, s>>>(a.arrived, (int)L.groups);
-      DG_CUDA_TRY(cudaGetLastError());
+      cudaLaunchConfig_t zc = {};
+      zc.gridDim = dim3(1);
+      zc.blockDim = dim3(64);
+      zc.stream = s;
+      zc.attrs = at;  // programmatic dependent of the previous work on the stream as well
+      zc.numAttrs = 1;
+      DG_CUDA_TRY(cudaLaunchKernelEx(&zc, attn_zero_arrivals, a.arrived, (int)L.groups));
     }
   }
   DG_CUDA_TRY(cudaLaunchKernelEx(&cfg, attn_fwd_tc, tk_c, tv_c, tk_n, tv_n, tq, a));

@@ -710,11 +710,14 @@ __device__ __forceinline__ int consumer_tile(int u, int ra, int rb, int ks) {
 }
 
 
-// The flag words of the next vocab_pair launch -> 0. It lets its dependent
-// launch start at once; the dependent's griddepcontrol.wait returns after
-// this grid has finished and its stores are visible.
+// The flag words of the next vocab_pair launch -> 0. It is itself a
+// programmatic dependent of whatever precedes it on the stream: it lets its
+// own dependent start at once, then waits for its predecessor to finish
+// before it writes. The dependent's griddepcontrol.wait returns after this
+// grid has finished and its stores are visible.
 __global__ void vocab_zero_flags(uint32_t* f, int n) {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   for (int i = threadIdx.x; i < n; i += blockDim.x) f[i] = 0u;
 }
 
@@ -1527,8 +1530,16 @@ int vocab_tc_launch(const __nv_bfloat16* h, const __nv_bfloat16* emb, int C, int
   static const int coop = env_int("DG_VOCAB_COOP", 0);
   const bool reset_kernel = pairs && coop != 1;
   if (reset_kernel) {
-    vocab_zero_flags<<<1, 256, 0, s>>>((uint32_t*)flags, (int)(zero_bytes / 4));
-    DG_CUDA_TRY(cudaGetLastError());
+    cudaLaunchAttribute za[1];
+    za[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    za[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t zc = {};
+    zc.gridDim = dim3(1);
+    zc.blockDim = dim3(256);
+    zc.stream = s;
+    zc.attrs = za;
+    zc.numAttrs = 1;
+    DG_CUDA_TRY(cudaLaunchKernelEx(&zc, vocab_zero_flags, (uint32_t*)flags, (int)(zero_bytes / 4)));
   } else {
     DG_CUDA_TRY(cudaMemsetAsync(flags, 0, zero_bytes, s));
   }
