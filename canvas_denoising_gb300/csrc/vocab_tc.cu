@@ -8,7 +8,7 @@
 // in bf16 through a global ring (V x 512 bytes) to the CTAs that form S. E
 // is streamed from HBM once for the logits; the S product reads each E tile
 // again shortly after, from L2 where most of it is still resident (at V =
-// 262144, d = 2816: 1.76 GB of DRAM reads per call for a 1.48 GB table).
+// 262144, d = 2816: 1.71 GB of DRAM reads per call for a 1.48 GB table).
 //
 // Design.
 //  * Fixed per-row reference. softmax(l) = exp(l - R) / sum exp(l - R) for
@@ -143,8 +143,9 @@ Layout make_layout(const Plan& p, int d) {
   L.flags = o;
   // Flags, zeroed before each launch (bytes): tile published counts [n_vt] (a byte per tile in
   // 32-bit words), reference count, abort, overflow [256] (a byte per row), row keys [256] (u32),
-  // then the pacing counts [n_vt] (bytes in words; zeroed only when pacing is on). Kept small: a
-  // memset of up to 4096 bytes costs ~1.2 us back to back, a larger one ~4.1 us.
+  // then the pacing counts [n_vt] (bytes in words; zeroed only when pacing is on). Kept small:
+  // the one-CTA reset kernel writes them, and in the cooperative forms a memset of up to 4096
+  // bytes costs ~1.2 us back to back, a larger one ~4.1 us.
   L.flag_bytes = 2 * tile_words(p.n_vt) * 4 + kFlagFixed;
   o += up256(L.flag_bytes);
   L.smax = o; o += up256((size_t)p.n_a * 256 * 4);

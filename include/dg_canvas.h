@@ -144,7 +144,7 @@ DG_API size_t dg_canvas_attn_noalloc_max_scratch(void);
  * self-conditioning product. E is streamed from HBM once for the logits;
  * the self-conditioning product reads each E tile again shortly after, from
  * L2 where most of it is still resident (measured at V = 262144, d = 2816:
- * 1.76 GB of DRAM reads per call for a 1.48 GB table).
+ * 1.71 GB of DRAM reads per call for a 1.48 GB table).
  * The step runs one CTA on every SM, all resident at once, with bounded
  * waits between them: run it when other kernels do not hold SMs for long
  * (a wait that expires, after about two seconds, sets DG_ERR_TIMEOUT in the
