@@ -47,3 +47,20 @@ def test_two_rank_aggregation_on_gloo():
 def test_single_process_helpers():
     assert bench.max_over_ranks(12.5) == 12.5
     assert bench.job_rate(1, 1000, 500.0) == pytest.approx(2000.0)
+
+
+def test_vocab_kernel_count_follows_the_launch_form(monkeypatch):
+    """The benchmark's kernel count per vocabulary step (its gpu_launches claim): the paired form
+    launches a flag reset kernel, the paired kernel and the combine; DG_VOCAB_COOP=1 replaces the
+    reset kernel by a memset; fp32 runs a kernel and the re-noise (plans are host-only queries)."""
+    from canvas_denoising_gb300 import binding as B
+    from canvas_denoising_gb300.configs import WORKLOADS
+    from canvas_denoising_gb300 import build as build_mod
+    build_mod.build()  # the host-side plan query needs the built library, not a GPU
+    B.load()
+    w = WORKLOADS["v262k_d2816_p4k"]
+    monkeypatch.delenv("DG_VOCAB_COOP", raising=False)
+    assert bench.vocab_kernels_per_call(B, w, torch.bfloat16) == 3
+    monkeypatch.setenv("DG_VOCAB_COOP", "1")
+    assert bench.vocab_kernels_per_call(B, w, torch.bfloat16) == 2
+    assert bench.vocab_kernels_per_call(B, WORKLOADS["tiny_f32"], torch.float32) == 2
